@@ -1,0 +1,223 @@
+/*
+ * wfst_gb300.h — C ABI of the GB300 (sm_103a) WFST beam-search decoder for
+ * CTC speech recognition.
+ *
+ * The decoder follows the page "GPU WFST Beam-Search Decoder" (OASR
+ * documentation, wfst_decoder_gpu).  Section numbers below are that page's.
+ * It takes per-frame log-posteriors log_prob[B, T, V] and a decoding graph
+ * (epsilon-free HLG style, or TLG style with epsilon arcs) and returns, per
+ * utterance, the best word sequence and its score, optionally an
+ * output_beam-pruned lattice, and, in streaming mode, a partial hypothesis
+ * per chunk.
+ *
+ * Conventions shared by every entry point
+ *   - Return value: WFST_OK (0) on success, a negative WFST_ERR_* code
+ *     otherwise; wfst_last_error() then holds a message (thread-local).
+ *   - Device pointers are CUDA device addresses on the decoder's device; host
+ *     pointers are plain (pageable or pinned) host memory.  "stream" is a
+ *     cudaStream_t passed as void* (NULL = the legacy default stream).
+ *   - Calls on one decoder are serialised by an internal mutex (§10: an
+ *     instance is thread-safe but serial); use one decoder per concurrent
+ *     caller.
+ *   - A lane whose capacity was exceeded is not an error: its meta[2]
+ *     overflow bits are set (§7 "Overflow bits") and its result may be
+ *     degraded; re-run it with larger capacities (decoding is idempotent).
+ *   - Exact-score ties are broken by the LOWEST arc id (final-state ties by
+ *     the lowest state), so results are deterministic and bit-exact with the
+ *     CPU reference.  (§3 leaves ties to atomic scheduling.)
+ */
+#ifndef WFST_GB300_H
+#define WFST_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define WFST_OK 0
+#define WFST_ERR_INVALID_ARG (-1)   /* a bad pointer, size, stride, length or id   */
+#define WFST_ERR_CORRUPT_GRAPH (-2) /* graph failed validation (§4 loader checks)  */
+#define WFST_ERR_CUDA (-3)          /* a CUDA runtime call failed                  */
+#define WFST_ERR_OOM (-4)           /* device or host allocation failed            */
+#define WFST_ERR_CAPACITY (-5)      /* requested capacities exceed the int32 tables */
+#define WFST_ERR_TIMEOUT (-6)       /* a bounded device-side wait gave up           */
+#define WFST_ERR_STATE (-7)         /* call not valid in the object's current state */
+
+/* ---- log-prob element types ------------------------------------------ */
+#define WFST_F32 0
+#define WFST_F16 1 /* widened exactly to fp32 inside (§11 "fp16") */
+
+/* ---- per-lane overflow bits (meta[3*b + 2]; §7 "Overflow bits") ------- */
+#define WFST_OVF_ARENA 4     /* winners log or lattice arena full            */
+#define WFST_OVF_KEPT 16     /* surviving frontier larger than frontier_cap  */
+#define WFST_OVF_PATH 32     /* best path longer than path_cap (oldest arcs lost) */
+
+/* ---- lattice record flags -------------------------------------------- */
+#define WFST_REC_EPS 1
+#define WFST_REC_FINAL 2
+#define WFST_REC_REDIRECT 4
+
+typedef struct wfst_graph wfst_graph;     /* opaque: device-resident graph, refcounted */
+typedef struct wfst_decoder wfst_decoder; /* opaque: workspace + lanes + streaming channels */
+
+/*
+ * Graph description (host arrays, borrowed only for the duration of
+ * wfst_graph_upload).  CSR by source state, arcs sorted by source; the arc
+ * index a in [0, num_arcs) is the arc id used everywhere (results, ties,
+ * lattice records) — the library never renumbers arcs (§4 "Identity arc
+ * order").
+ */
+typedef struct {
+  int32_t num_states;          /* N > 0 */
+  int32_t start_state;         /* in [0, N) */
+  int32_t vocab_size;          /* V in [1, 65535): ilabels are stored as u16 (§4) */
+  int32_t reserved;
+  int64_t num_arcs;            /* A >= 0, A + N < 2^31 */
+  const int64_t* row_splits;   /* [N+1], row_splits[0] = 0, monotone, row_splits[N] = A */
+  const int32_t* ilabel;       /* [A] -1 = epsilon (consumes no frame), 0 = blank, 1..V-1 */
+  const int32_t* olabel;       /* [A] output word id, 0 = none */
+  const float* weight;         /* [A] log-semiring score added on the arc (higher is better) */
+  const int32_t* dst;          /* [A] in [0, N) */
+  const float* final_weight;   /* [N] final score, -INFINITY = not final */
+} wfst_graph_desc;
+
+typedef struct {
+  float search_beam;      /* k2 search beam (§3 "Dynamic beam") */
+  float output_beam;      /* lattice backward prune only (§3) */
+  int32_t min_active;     /* soft lower frontier target */
+  int32_t max_active;     /* soft upper frontier target (beam decay only, never top-k) */
+  int32_t allow_partial;  /* 1: without a final state, return the best frontier token */
+  int32_t lattice;        /* 1: persist candidates for wfst_lattice_export */
+  int32_t streaming;      /* 1: decoder serves wfst_stream_* (online beam semantics) */
+} wfst_params;
+
+/* Per-lane capacities; 0 in any field selects its default. */
+typedef struct {
+  int64_t frontier_cap;   /* tokens per lane per frame (default: num_states, never overflows) */
+  int64_t log_cap;        /* winners-log entries per lane (default (max_frames+2)*4*max_active, >= 1Mi) */
+  int64_t lattice_cap;    /* lattice records per lane (default (max_frames+2)*2*max_active) */
+  int64_t path_cap;       /* arcs of one best path (default 4*(max_frames+2)) */
+} wfst_capacity;
+
+typedef struct {
+  int32_t t;          /* frame of the source node (epsilon and final records: the frame they sit in) */
+  int32_t src_state;
+  int32_t dst_state;  /* -1 = super-final node */
+  int32_t arc_id;     /* arc id; num_arcs + s for the final (or redirect) record of state s */
+  int32_t flags;      /* WFST_REC_* */
+  float score;        /* the record's own score: weight + log_prob, weight, or final weight */
+} wfst_lat_record;
+
+/*
+ * Upload and validate a graph on `device` (§4 "Graph Image": every index the
+ * decoder follows is checked — start state, monotone row_splits, arc
+ * destinations, label ranges, acyclic epsilon subgraph, finite weights).
+ * On success *out owns one reference.  Errors: INVALID_ARG (NULL pointers),
+ * CORRUPT_GRAPH (validation), CUDA, OOM.
+ */
+int wfst_graph_upload(const wfst_graph_desc* desc, int32_t device, wfst_graph** out);
+
+/* out[0..7] = {num_states, num_arcs, vocab_size, start_state, has_epsilon,
+ *              epsilon depth (longest epsilon path), device bytes, device} */
+int wfst_graph_info(const wfst_graph* g, int64_t* out);
+
+/* Drop the caller's reference; device arrays live on while a decoder holds
+ * the graph (§10: a decoder co-owns its graph). */
+void wfst_graph_free(wfst_graph* g);
+
+/*
+ * Create a decoder with max_lanes lanes (utterances decoded together, or
+ * streaming channels) for frames up to max_frames per lane (offline: per
+ * call; streaming: per channel when lattice is on).  caps may be NULL.
+ * All workspace is allocated here, once; decoding allocates nothing more
+ * except a host-input staging buffer (see wfst_decode).
+ * Errors: INVALID_ARG, CAPACITY (a table would exceed 2^31 entries), OOM, CUDA.
+ */
+int wfst_decoder_create(wfst_graph* g, const wfst_params* params, int32_t max_lanes,
+                        int32_t max_frames, const wfst_capacity* caps, wfst_decoder** out);
+void wfst_decoder_free(wfst_decoder* d);
+
+/*
+ * Offline batched decode (§1, §3, §7).  log_probs: [B, T, V] elements of
+ * `dtype`, element (b, t, v) at log_probs[b*stride_b + t*stride_t + v]
+ * (unit stride over v, stride_t >= V).  It may be a device pointer (read in
+ * place) or a host pointer (copied to device inside the call).  lens: host
+ * [B], 0 <= lens[b] <= T.  Requires B <= max_lanes, T <= max_frames and a
+ * decoder created with streaming = 0.
+ * Outputs (host, caller-allocated): words [B*words_cap] (lane b's words at
+ * b*words_cap, forward order), word_lens [B] (TRUE length, may exceed
+ * words_cap: re-issue with a larger buffer), scores [B] (fp32 path score
+ * widened), meta [B*3] = {ok, reached_final, overflow bits}.
+ * The call is stream-ordered on `stream` and returns after the results are
+ * on the host.  Errors: INVALID_ARG, STATE, CUDA, TIMEOUT.
+ */
+int wfst_decode(wfst_decoder* d, const void* log_probs, int32_t dtype, int64_t stride_b,
+                int64_t stride_t, const int32_t* lens, int32_t B, int32_t T, void* stream,
+                int32_t* words, int32_t words_cap, int32_t* word_lens, double* scores,
+                int32_t* meta);
+
+/*
+ * Lattice of one lane after wfst_decode or wfst_stream_finalize with
+ * params.lattice = 1: every in-beam candidate (emitting, epsilon, final,
+ * redirect) whose best complete path is within output_beam of the best path
+ * (§3 "output_beam ... applied by the lattice backward prune only"; §7).
+ * Records are sorted by (t, src_state, arc_id).  *n_records receives the
+ * true count; at most `cap` records are written.  Errors: INVALID_ARG, STATE.
+ */
+int wfst_lattice_export(wfst_decoder* d, int32_t lane, wfst_lat_record* out, int64_t cap,
+                        int64_t* n_records);
+
+/* ---- streaming (§8 "Streaming Lifecycle"); decoder created with streaming = 1 */
+
+/* Claim a free channel (= lane) and open its start frontier; *channel = -1
+ * when every channel is busy. */
+int wfst_stream_create(wfst_decoder* d, int32_t* channel);
+
+/*
+ * Advance n channels by their next chunk: log_probs [n, chunk_T, V] (device
+ * or host, strides as in wfst_decode), chunk_lens host [n] in [0, chunk_T].
+ * Online beam semantics: the offline last-frames rule never fires (§3).
+ * If want_partial, the outputs receive each channel's best current
+ * hypothesis (§8: from the best current-frontier token), laid out as in
+ * wfst_decode (meta reached_final is 0); otherwise they may be NULL.
+ */
+int wfst_stream_advance(wfst_decoder* d, const int32_t* channels, int32_t n,
+                        const void* log_probs, int32_t dtype, int64_t stride_b, int64_t stride_t,
+                        const int32_t* chunk_lens, int32_t chunk_T, int32_t want_partial,
+                        void* stream, int32_t* words, int32_t words_cap, int32_t* word_lens,
+                        double* scores, int32_t* meta);
+
+/* Final step + backtrack (+ lattice prune) of n channels; outputs as in
+ * wfst_decode.  The channels stay claimed until wfst_stream_release. */
+int wfst_stream_finalize(wfst_decoder* d, const int32_t* channels, int32_t n, void* stream,
+                         int32_t* words, int32_t words_cap, int32_t* word_lens, double* scores,
+                         int32_t* meta);
+
+/* Return a channel to the pool (its lattice is discarded). */
+int wfst_stream_release(wfst_decoder* d, int32_t channel);
+
+/*
+ * Counters of the last decode / stream call (host int64, n entries written,
+ * at most WFST_STAT_COUNT): see WFST_STAT_* for the order.
+ */
+#define WFST_STAT_FRAMES 0        /* frames consumed (sum over lanes) */
+#define WFST_STAT_ARCS 1          /* arcs expanded: emitting + epsilon relaxations + final arcs */
+#define WFST_STAT_SUM_N 2         /* sum over lane-steps of the frontier size */
+#define WFST_STAT_SUM_D 3         /* sum of emitting arcs expanded */
+#define WFST_STAT_SUM_A 4         /* sum of admitted emitting candidates */
+#define WFST_STAT_SUM_M 5         /* sum of next-frontier sizes (after closure) */
+#define WFST_STAT_EPS 6           /* epsilon arcs relaxed (once per closure token) */
+#define WFST_STAT_STEPS 7         /* grid steps of the device loop */
+#define WFST_STAT_BARRIERS 8      /* grid barriers executed */
+#define WFST_STAT_KERNEL_NS 9     /* device time of the decode kernel (ns) */
+#define WFST_STAT_COUNT 10
+int wfst_stats(wfst_decoder* d, int64_t* out, int32_t n);
+
+const char* wfst_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WFST_GB300_H */

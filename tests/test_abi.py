@@ -1,0 +1,77 @@
+"""The C ABI library builds, loads and exports every entry point the header
+declares (no GPU needed: nothing here launches device work)."""
+import os
+import re
+import subprocess
+
+import pytest
+
+import wfst_beam_search_gb300 as W
+from wfst_beam_search_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "wfst_gb300.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(wfst_[a-z_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return W.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["wfst_graph_upload", "wfst_decode", "wfst_lattice_export", "wfst_stream_create",
+              "wfst_stream_advance", "wfst_stream_finalize", "wfst_stream_release"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (wfst_[a-z_]+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_binding_uses_the_c_names():
+    for n in declared_functions():
+        assert hasattr(W, n), n
+
+
+def test_last_error_and_argument_checks_without_gpu(lib):
+    # NULL arguments are rejected on the host before any CUDA call
+    assert lib.wfst_graph_upload(None, 0, None) == -1
+    assert b"NULL" in lib.wfst_last_error()
+    assert lib.wfst_decode(None, None, 0, 0, 0, None, 0, 0, None, None, 0, None, None, None) == -1
+
+
+def test_graph_validation_rejects_corrupt_graphs_on_host(lib):
+    import ctypes as C
+    import numpy as np
+    import synth
+    # epsilon cycle -> CORRUPT_GRAPH before any device allocation
+    g = synth.graph_from_arcs(3, 2, np.array([0, 1, 2]), [1, 2, 0], [-1, -1, -1], [0, 0, 0],
+                              [0.0, 0.0, 0.0], np.zeros(3, np.float32))
+    for bad, msg in [(g, b"cycle")]:
+        keep = [np.ascontiguousarray(bad[k]) for k in ("row_splits", "ilabel", "olabel",
+                                                       "weight", "dst", "final")]
+        desc = W.GraphDesc(3, 0, 2, 0, 3, *[k.ctypes.data_as(C.c_void_p) for k in keep])
+        h = C.c_void_p()
+        assert lib.wfst_graph_upload(C.byref(desc), 0, C.byref(h)) == -2
+        assert msg in lib.wfst_last_error()
+    # vocab too large for u16 labels
+    keep = [np.ascontiguousarray(g[k]) for k in ("row_splits", "ilabel", "olabel", "weight",
+                                                 "dst", "final")]
+    desc = W.GraphDesc(3, 0, 70000, 0, 3, *[k.ctypes.data_as(C.c_void_p) for k in keep])
+    h = C.c_void_p()
+    assert lib.wfst_graph_upload(C.byref(desc), 0, C.byref(h)) == -2
+    assert b"vocab" in lib.wfst_last_error()

@@ -1,0 +1,258 @@
+"""GPU parity: the CUDA decoder (through the C ABI) against the CPU oracle on
+the same seeded inputs.  Words, reached-final flags, ok flags and lattice
+record sets must be identical; scores within 1e-4 absolute."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.gpu_common import (assert_lane_equal, assert_lattice_equal, gpu_decoder, oracle_lane,
+                              wl_params)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def W():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import wfst_beam_search_gb300 as W
+    W.load()
+    return W
+
+
+def _cuda(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).to("cuda:0")
+
+
+# ------------------------------------------------------------ tiny random graphs
+
+def _tiny_case(seed, p_eps):
+    rng = np.random.default_rng(77000 + seed)
+    N = int(rng.integers(2, 40))
+    V = int(rng.integers(2, 9))
+    g = synth.random_tiny_graph(rng, N, V, max_deg=int(rng.integers(1, 6)), p_eps=p_eps,
+                                dyadic=bool(seed % 2 == 0), allow_empty=bool(seed % 3 == 0),
+                                p_final=float(rng.choice([0.0, 0.2, 0.6])))
+    B = 4
+    T = int(rng.integers(1, 14))
+    lens = rng.integers(0, T + 1, size=B).astype(np.int32)
+    lens[0] = T
+    if seed % 2 == 0:
+        lp = np.stack([synth.dyadic_log_probs(rng, T, V, lo=-4.0) for _ in range(B)])
+    else:
+        lp = np.log(rng.dirichlet(np.ones(V), size=(B, T))).astype(np.float32)
+    p = dict(search_beam=float(rng.choice([1.0, 2.5, 6.0, 20.0])), output_beam=float(rng.choice([0.0, 1.0, 4.0])),
+             min_active=int(rng.integers(0, 5)), max_active=int(rng.integers(1, 12)),
+             allow_partial=bool(seed % 5 != 0), lattice=True)
+    return g, lp, lens, p
+
+
+@pytest.mark.parametrize("p_eps", [0.0, 0.3])
+def test_tiny_random_graphs(W, p_eps):
+    for seed in range(60):
+        g, lp, lens, p = _tiny_case(seed, p_eps)
+        G, D = gpu_decoder(W, g, p, max_lanes=6, max_frames=lp.shape[1])
+        OG = oracle.Graph(g)
+        out = D.decode(_cuda(lp), lens)
+        for b in range(len(lens)):
+            ref = oracle_lane(OG, lp[b], lens[b], p)
+            where = f"seed {seed} eps {p_eps} lane {b}"
+            assert_lane_equal(out[b], ref, where)
+            if ref["ok"]:
+                assert_lattice_equal(D.lattice(b), ref["lattice"], where)
+        D.close()
+        G.close()
+
+
+def test_epsilon_first_arc_order(W):
+    """Arcs of each state with epsilon arcs FIRST: the decoder re-lays arcs out
+    internally but must report the caller's arc ids and break ties on them."""
+    for seed in range(30):
+        g, lp, lens, p = _tiny_case(seed, 0.4)
+        rs = g["row_splits"]
+        perm = np.concatenate([np.concatenate([np.arange(rs[s], rs[s + 1])[g["ilabel"][rs[s]:rs[s + 1]] < 0],
+                                               np.arange(rs[s], rs[s + 1])[g["ilabel"][rs[s]:rs[s + 1]] >= 0]])
+                               for s in range(g["num_states"])]).astype(np.int64)
+        g2 = dict(g)
+        for k in ("ilabel", "olabel", "weight", "dst"):
+            g2[k] = np.ascontiguousarray(g[k][perm])
+        G, D = gpu_decoder(W, g2, p, max_lanes=4, max_frames=lp.shape[1])
+        OG = oracle.Graph(g2)
+        out = D.decode(_cuda(lp), lens)
+        for b in range(len(lens)):
+            ref = oracle_lane(OG, lp[b], lens[b], p)
+            assert_lane_equal(out[b], ref, f"eps-first seed {seed} lane {b}")
+            if ref["ok"]:
+                assert_lattice_equal(D.lattice(b), ref["lattice"], f"eps-first seed {seed} lane {b}")
+        D.close()
+        G.close()
+
+
+# ------------------------------------------------------------ the five workloads
+
+@pytest.fixture(scope="module")
+def graphs():
+    cache = {}
+
+    def get(i):
+        if i not in cache:
+            cache[i] = synth.make_graph(i)
+        return cache[i]
+    return get
+
+
+def test_workload0_tiny_with_lattice(W, graphs):
+    wl = synth.workload(0)
+    g = graphs(0)
+    lp = synth.make_log_probs(0)
+    lens = synth.make_lens(0)
+    p = wl_params(wl)
+    G, D = gpu_decoder(W, g, p, wl.B, wl.T)
+    out = D.decode(_cuda(lp), lens)
+    ref = oracle_lane(oracle.Graph(g), lp[0], lens[0], p)
+    assert_lane_equal(out[0], ref, "workload 0")
+    assert_lattice_equal(D.lattice(0), ref["lattice"], "workload 0")
+    st = D.stats()
+    assert st["arcs_expanded"] == ref["stats"]["arcs_expanded"]
+    assert st["sum_a"] == ref["stats"]["sum_a"]
+
+
+def test_workload1_all_lanes(W, graphs):
+    wl = synth.workload(1)
+    g = graphs(1)
+    lp = synth.make_log_probs(1)
+    lens = synth.make_lens(1)
+    p = wl_params(wl)
+    G, D = gpu_decoder(W, g, p, wl.B, wl.T)
+    out = D.decode(_cuda(lp), lens)
+    OG = oracle.Graph(g)
+    refs = oracle.decode_batch(OG, lp, lens, oracle.params(**p), threads=8)
+    arcs = 0
+    for b in range(wl.B):
+        assert_lane_equal(out[b], refs[b], f"workload 1 lane {b}")
+        arcs += refs[b]["stats"]["arcs_expanded"]
+    assert D.stats()["arcs_expanded"] == arcs
+    # fp32 input from the host gives the same result
+    out2 = D.decode(lp, lens)
+    for b in range(wl.B):
+        assert_lane_equal(out2[b], refs[b], f"workload 1 host input lane {b}")
+
+
+def test_workload3_tlg_epsilon(W, graphs):
+    wl = synth.workload(3)
+    g = graphs(3)
+    lp = synth.make_log_probs(3)
+    lens = synth.make_lens(3)
+    p = wl_params(wl)
+    G, D = gpu_decoder(W, g, p, wl.B, wl.T)
+    assert G.has_eps
+    out = D.decode(_cuda(lp), lens)
+    OG = oracle.Graph(g)
+    lanes = [0, 7, 19, 31]
+    refs = oracle.decode_batch(OG, lp[lanes], lens[lanes], oracle.params(**p), threads=4)
+    for k, b in enumerate(lanes):
+        assert_lane_equal(out[b], refs[k], f"workload 3 lane {b}")
+    assert all(o["ok"] for o in out)
+
+
+def test_workload2_hlg_sampled(W, graphs):
+    wl = synth.workload(2)
+    g = graphs(2)
+    lp = synth.make_log_probs(2)
+    lens = synth.make_lens(2)
+    p = wl_params(wl)
+    G, D = gpu_decoder(W, g, p, wl.B, wl.T)
+    out = D.decode(_cuda(lp), lens)
+    OG = oracle.Graph(g)
+    lanes = [0, 33, 63]
+    refs = oracle.decode_batch(OG, lp[lanes], lens[lanes], oracle.params(**p), threads=3)
+    for k, b in enumerate(lanes):
+        assert_lane_equal(out[b], refs[k], f"workload 2 lane {b}")
+    assert all(o["ok"] and o["overflow"] == 0 for o in out)
+    # decoding is idempotent
+    out2 = D.decode(_cuda(lp), lens)
+    for b in range(wl.B):
+        assert list(out2[b]["words"]) == list(out[b]["words"]) and out2[b]["score"] == out[b]["score"]
+
+
+# ------------------------------------------------------------ edge cases
+
+def test_edge_lengths_and_batch_composition(W, graphs):
+    wl = synth.workload(1)
+    g = graphs(1)
+    lp = synth.make_log_probs(1, lanes=range(6), T=40)
+    p = wl_params(wl)
+    G, D = gpu_decoder(W, g, p, 8, 40)
+    OG = oracle.Graph(g)
+    lens = np.array([40, 0, 1, 17, 39, 40], np.int32)
+    out = D.decode(_cuda(lp), lens)
+    for b in range(6):
+        assert_lane_equal(out[b], oracle_lane(OG, lp[b], lens[b], p), f"edge lane {b}")
+    # one lane alone equals the same lane inside the batch
+    solo = D.decode(_cuda(lp[3:4]), lens[3:4])
+    assert list(solo[0]["words"]) == list(out[3]["words"]) and solo[0]["score"] == out[3]["score"]
+    # T = 0
+    out0 = D.decode(_cuda(lp[:2, :0]), np.zeros(2, np.int32))
+    for b in range(2):
+        assert_lane_equal(out0[b], oracle_lane(OG, lp[b], 0, p), f"T=0 lane {b}")
+
+
+def test_fp16_input_matches_oracle_on_widened_values(W, graphs):
+    wl = synth.workload(1)
+    g = graphs(1)
+    lp16 = synth.make_log_probs(1, lanes=range(4), T=60).astype(np.float16)
+    lens = np.full(4, 60, np.int32)
+    p = wl_params(wl)
+    G, D = gpu_decoder(W, g, p, 4, 60)
+    out = D.decode(_cuda(lp16), lens)
+    OG = oracle.Graph(g)
+    for b in range(4):
+        assert_lane_equal(out[b], oracle_lane(OG, lp16[b].astype(np.float32), 60, p), f"fp16 lane {b}")
+
+
+def test_no_final_state_allow_partial_off(W):
+    # chain without any final state
+    T, V = 6, 3
+    g = synth.graph_from_arcs(T + 1, V, np.arange(T), np.arange(1, T + 1), np.ones(T, np.int32),
+                              np.arange(1, T + 1), -0.5 * np.ones(T), np.full(T + 1, -np.inf, np.float32))
+    lp = np.full((2, T, V), -1.0, np.float32)
+    lens = np.array([T, 3], np.int32)
+    for ap in (True, False):
+        p = dict(search_beam=10.0, output_beam=5.0, min_active=0, max_active=100, allow_partial=ap,
+                 lattice=True)
+        G, D = gpu_decoder(W, g, p, 2, T)
+        out = D.decode(_cuda(lp), lens)
+        OG = oracle.Graph(g)
+        for b in range(2):
+            ref = oracle_lane(OG, lp[b], lens[b], p)
+            assert_lane_equal(out[b], ref, f"no-final ap={ap} lane {b}")
+            if ref["ok"]:
+                assert_lattice_equal(D.lattice(b), ref["lattice"], f"no-final lattice lane {b}")
+
+
+def test_capacity_overflow_is_flagged_and_recovers(W, graphs):
+    wl = synth.workload(1)
+    g = graphs(1)
+    lp = synth.make_log_probs(1, lanes=range(2), T=50)
+    lens = np.full(2, 50, np.int32)
+    p = wl_params(wl)
+    caps = W.Capacity(64, 0, 0, 0)      # frontier of at most 64 tokens per frame
+    G, D = gpu_decoder(W, g, p, 2, 50, caps=caps)
+    out = D.decode(_cuda(lp), lens)
+    assert all(o["overflow"] & W.OVF_KEPT for o in out)
+    # a full-capacity decoder on the same graph is unaffected, and a small
+    # utterance on the overflowed decoder decodes exactly afterwards
+    lens_small = np.array([1, 2], np.int32)
+    out2 = D.decode(_cuda(lp), lens_small)
+    OG = oracle.Graph(g)
+    for b in range(2):
+        ref = oracle_lane(OG, lp[b], lens_small[b], p)
+        if out2[b]["overflow"] == 0:
+            assert_lane_equal(out2[b], ref, f"after overflow lane {b}")
+    caps = W.Capacity(0, 1000, 0, 0)    # winners log too small
+    G2, D2 = gpu_decoder(W, g, p, 2, 50, caps=caps, graph=G)
+    out3 = D2.decode(_cuda(lp), lens)
+    assert all(o["overflow"] & W.OVF_ARENA for o in out3)

@@ -1,0 +1,349 @@
+"""Python binding of the GB300 WFST beam-search decoder's C ABI.
+
+The functions below carry the C names (``wfst_graph_upload``, ``wfst_decode``,
+...) and only marshal arguments: every step of the decode runs in the CUDA
+library ``_build/libwfst_gb300.so`` (see ``include/wfst_gb300.h``).  There is
+no CPU fallback; loading fails loudly when the library is missing.
+
+``Graph`` and ``Decoder`` wrap the handles for convenience.  Device buffers
+may be torch CUDA tensors (pointer + strides are passed through) or numpy
+arrays (host input: the library copies them to the device inside the call).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+import numpy as np
+
+from . import _build
+
+WFST_OK = 0
+WFST_F32, WFST_F16 = 0, 1
+OVF_ARENA, OVF_KEPT, OVF_PATH = 4, 16, 32
+REC_EPS, REC_FINAL, REC_REDIRECT = 1, 2, 4
+STAT_NAMES = ["frames", "arcs_expanded", "sum_n", "sum_D", "sum_a", "sum_m", "eps",
+              "steps", "barriers", "kernel_ns"]
+ERRORS = {-1: "INVALID_ARG", -2: "CORRUPT_GRAPH", -3: "CUDA", -4: "OOM", -5: "CAPACITY",
+          -6: "TIMEOUT", -7: "STATE"}
+
+LAT_DTYPE = np.dtype([("t", "<i4"), ("src_state", "<i4"), ("dst_state", "<i4"),
+                      ("arc_id", "<i4"), ("flags", "<i4"), ("score", "<f4")])
+
+EXPORTED = ["wfst_graph_upload", "wfst_graph_info", "wfst_graph_free", "wfst_decoder_create",
+            "wfst_decoder_free", "wfst_decode", "wfst_lattice_export", "wfst_stream_create",
+            "wfst_stream_advance", "wfst_stream_finalize", "wfst_stream_release", "wfst_stats",
+            "wfst_last_error"]
+
+
+class WfstError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"{ERRORS.get(code, code)}: {msg}")
+        self.code = code
+
+
+class GraphDesc(C.Structure):
+    _fields_ = [("num_states", C.c_int32), ("start_state", C.c_int32),
+                ("vocab_size", C.c_int32), ("reserved", C.c_int32), ("num_arcs", C.c_int64),
+                ("row_splits", C.c_void_p), ("ilabel", C.c_void_p), ("olabel", C.c_void_p),
+                ("weight", C.c_void_p), ("dst", C.c_void_p), ("final_weight", C.c_void_p)]
+
+
+class Params(C.Structure):
+    _fields_ = [("search_beam", C.c_float), ("output_beam", C.c_float),
+                ("min_active", C.c_int32), ("max_active", C.c_int32),
+                ("allow_partial", C.c_int32), ("lattice", C.c_int32), ("streaming", C.c_int32)]
+
+
+class Capacity(C.Structure):
+    _fields_ = [("frontier_cap", C.c_int64), ("log_cap", C.c_int64),
+                ("lattice_cap", C.c_int64), ("path_cap", C.c_int64)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False):
+    """Load the CUDA library (raises if it is not built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if build_if_missing and not _build.up_to_date():
+            _build.build()
+        if not os.path.exists(_build.LIB):
+            raise ImportError("libwfst_gb300.so is not built; run __graft_entry__.build() "
+                              "(the decoder has no CPU fallback)")
+        L = C.CDLL(_build.LIB)
+        P, i32, i64 = C.c_void_p, C.c_int32, C.c_int64
+        L.wfst_last_error.restype = C.c_char_p
+        L.wfst_graph_upload.argtypes = [C.POINTER(GraphDesc), i32, C.POINTER(P)]
+        L.wfst_graph_info.argtypes = [P, P]
+        L.wfst_graph_free.argtypes = [P]
+        L.wfst_graph_free.restype = None
+        L.wfst_decoder_create.argtypes = [P, C.POINTER(Params), i32, i32, C.POINTER(Capacity),
+                                          C.POINTER(P)]
+        L.wfst_decoder_free.argtypes = [P]
+        L.wfst_decoder_free.restype = None
+        L.wfst_decode.argtypes = [P, P, i32, i64, i64, P, i32, i32, P, P, i32, P, P, P]
+        L.wfst_lattice_export.argtypes = [P, i32, P, i64, C.POINTER(i64)]
+        L.wfst_stream_create.argtypes = [P, C.POINTER(i32)]
+        L.wfst_stream_advance.argtypes = [P, P, i32, P, i32, i64, i64, P, i32, i32, P, P, i32, P,
+                                          P, P]
+        L.wfst_stream_finalize.argtypes = [P, P, i32, P, P, i32, P, P, P]
+        L.wfst_stream_release.argtypes = [P, i32]
+        L.wfst_stats.argtypes = [P, P, i32]
+        for name in EXPORTED:
+            if name not in ("wfst_last_error", "wfst_graph_free", "wfst_decoder_free"):
+                getattr(L, name).restype = C.c_int
+        _lib = L
+        return _lib
+
+
+def _check(rc):
+    if rc != WFST_OK:
+        raise WfstError(rc, load().wfst_last_error().decode())
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    if isinstance(a, np.ndarray):
+        return a.ctypes.data_as(C.c_void_p)
+    return C.c_void_p(int(a.data_ptr()))   # torch tensor
+
+
+# ------------------------------------------------------------ raw C entry points
+
+def wfst_last_error() -> str:
+    return load().wfst_last_error().decode()
+
+
+def wfst_graph_upload(desc: GraphDesc, device: int):
+    h = C.c_void_p()
+    _check(load().wfst_graph_upload(C.byref(desc), device, C.byref(h)))
+    return h
+
+
+def wfst_graph_info(h):
+    out = np.zeros(8, np.int64)
+    _check(load().wfst_graph_info(h, _ptr(out)))
+    return out
+
+
+def wfst_graph_free(h):
+    load().wfst_graph_free(h)
+
+
+def wfst_decoder_create(graph_h, params: Params, max_lanes: int, max_frames: int, caps=None):
+    h = C.c_void_p()
+    _check(load().wfst_decoder_create(graph_h, C.byref(params), max_lanes, max_frames,
+                                      C.byref(caps) if caps is not None else None, C.byref(h)))
+    return h
+
+
+def wfst_decoder_free(h):
+    load().wfst_decoder_free(h)
+
+
+def wfst_decode(h, lp_ptr, dtype, stride_b, stride_t, lens_ptr, B, T, stream, words_ptr,
+                words_cap, word_lens_ptr, scores_ptr, meta_ptr):
+    _check(load().wfst_decode(h, lp_ptr, dtype, stride_b, stride_t, lens_ptr, B, T, stream,
+                              words_ptr, words_cap, word_lens_ptr, scores_ptr, meta_ptr))
+
+
+def wfst_lattice_export(h, lane, out_ptr, cap):
+    n = C.c_int64()
+    _check(load().wfst_lattice_export(h, lane, out_ptr, cap, C.byref(n)))
+    return n.value
+
+
+def wfst_stream_create(h):
+    ch = C.c_int32()
+    _check(load().wfst_stream_create(h, C.byref(ch)))
+    return ch.value
+
+
+def wfst_stream_advance(h, ch_ptr, n, lp_ptr, dtype, stride_b, stride_t, lens_ptr, chunk_T,
+                        want_partial, stream, words_ptr, words_cap, word_lens_ptr, scores_ptr,
+                        meta_ptr):
+    _check(load().wfst_stream_advance(h, ch_ptr, n, lp_ptr, dtype, stride_b, stride_t, lens_ptr,
+                                      chunk_T, want_partial, stream, words_ptr, words_cap,
+                                      word_lens_ptr, scores_ptr, meta_ptr))
+
+
+def wfst_stream_finalize(h, ch_ptr, n, stream, words_ptr, words_cap, word_lens_ptr, scores_ptr,
+                         meta_ptr):
+    _check(load().wfst_stream_finalize(h, ch_ptr, n, stream, words_ptr, words_cap, word_lens_ptr,
+                                       scores_ptr, meta_ptr))
+
+
+def wfst_stream_release(h, ch):
+    _check(load().wfst_stream_release(h, ch))
+
+
+def wfst_stats(h):
+    out = np.zeros(len(STAT_NAMES), np.int64)
+    _check(load().wfst_stats(h, _ptr(out), len(STAT_NAMES)))
+    return dict(zip(STAT_NAMES, out.tolist()))
+
+
+# ------------------------------------------------------------ convenience wrappers
+
+class Graph:
+    """Device graph uploaded from a CSR dict (keys as produced by ``synth``)."""
+
+    def __init__(self, g: dict, device: int = 0):
+        keep = dict(
+            row_splits=np.ascontiguousarray(g["row_splits"], dtype=np.int64),
+            ilabel=np.ascontiguousarray(g["ilabel"], dtype=np.int32),
+            olabel=np.ascontiguousarray(g["olabel"], dtype=np.int32),
+            weight=np.ascontiguousarray(g["weight"], dtype=np.float32),
+            dst=np.ascontiguousarray(g["dst"], dtype=np.int32),
+            final=np.ascontiguousarray(g["final"], dtype=np.float32),
+        )
+        desc = GraphDesc(int(g["num_states"]), int(g["start_state"]), int(g["vocab_size"]), 0,
+                         int(len(keep["ilabel"])), _ptr(keep["row_splits"]), _ptr(keep["ilabel"]),
+                         _ptr(keep["olabel"]), _ptr(keep["weight"]), _ptr(keep["dst"]),
+                         _ptr(keep["final"]))
+        self.h = wfst_graph_upload(desc, device)
+        self.device = device
+        info = wfst_graph_info(self.h)
+        self.num_states, self.num_arcs, self.vocab_size = int(info[0]), int(info[1]), int(info[2])
+        self.has_eps, self.eps_depth, self.device_bytes = bool(info[4]), int(info[5]), int(info[6])
+
+    def close(self):
+        if getattr(self, "h", None):
+            wfst_graph_free(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def make_params(search_beam=20.0, output_beam=8.0, min_active=30, max_active=10000,
+                allow_partial=True, lattice=False, streaming=False) -> Params:
+    return Params(float(search_beam), float(output_beam), int(min_active), int(max_active),
+                  int(bool(allow_partial)), int(bool(lattice)), int(bool(streaming)))
+
+
+def _lp_args(lp):
+    """(pointer, dtype code, stride_b, stride_t, B, T) of a [B, T, V] tensor."""
+    if isinstance(lp, np.ndarray):
+        if lp.dtype not in (np.float32, np.float16):
+            raise TypeError("log_probs must be float32 or float16")
+        dt = WFST_F16 if lp.dtype == np.float16 else WFST_F32
+        es = lp.itemsize
+        sb, st, sv = (s // es for s in lp.strides)
+    else:  # torch tensor
+        import torch
+        if lp.dtype not in (torch.float32, torch.float16):
+            raise TypeError("log_probs must be float32 or float16")
+        dt = WFST_F16 if lp.dtype == torch.float16 else WFST_F32
+        sb, st, sv = lp.stride()
+    if sv != 1:
+        raise ValueError("log_probs must have unit stride over the vocabulary")
+    return _ptr(lp), dt, int(sb), int(st), int(lp.shape[0]), int(lp.shape[1])
+
+
+class Decoder:
+    def __init__(self, graph: Graph, params: Params, max_lanes: int, max_frames: int,
+                 caps: Capacity | None = None):
+        self.graph = graph
+        self.params = params
+        self.max_lanes = max_lanes
+        self.max_frames = max_frames
+        self.h = wfst_decoder_create(graph.h, params, max_lanes, max_frames, caps)
+
+    def close(self):
+        if getattr(self, "h", None):
+            wfst_decoder_free(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def decode(self, lp, lens, stream=None, words_cap=4096):
+        """Offline decode of [B, T, V] log-probs (torch CUDA tensor or numpy)."""
+        ptr, dt, sb, st, B, T = _lp_args(lp)
+        lens = np.ascontiguousarray(lens, dtype=np.int32)
+        words = np.zeros((B, max(words_cap, 1)), np.int32)
+        wl = np.zeros(B, np.int32)
+        sc = np.zeros(B, np.float64)
+        meta = np.zeros((B, 3), np.int32)
+        wfst_decode(self.h, ptr, dt, sb, st, _ptr(lens), B, T, _stream(stream), _ptr(words),
+                    words_cap, _ptr(wl), _ptr(sc), _ptr(meta))
+        return [dict(words=words[b, : min(wl[b], words_cap)].copy(), n_words=int(wl[b]),
+                     score=float(sc[b]), ok=int(meta[b, 0]), reached_final=int(meta[b, 1]),
+                     overflow=int(meta[b, 2])) for b in range(B)]
+
+    def lattice(self, lane: int):
+        n = wfst_lattice_export(self.h, lane, None, 0)
+        out = np.zeros(n, LAT_DTYPE)
+        if n:
+            wfst_lattice_export(self.h, lane, _ptr(out), n)
+        return out
+
+    def stats(self):
+        return wfst_stats(self.h)
+
+    # streaming
+    def stream_create(self) -> int:
+        return wfst_stream_create(self.h)
+
+    def stream_advance(self, channels, lp, chunk_lens, want_partial=True, stream=None,
+                       words_cap=4096):
+        ch = np.ascontiguousarray(channels, dtype=np.int32)
+        n = len(ch)
+        ptr, dt, sb, st, B, T = _lp_args(lp)
+        if B != n:
+            raise ValueError("one log-prob row per channel")
+        cl = np.ascontiguousarray(chunk_lens, dtype=np.int32)
+        words = np.zeros((n, max(words_cap, 1)), np.int32)
+        wl = np.zeros(n, np.int32)
+        sc = np.zeros(n, np.float64)
+        meta = np.zeros((n, 3), np.int32)
+        wfst_stream_advance(self.h, _ptr(ch), n, ptr, dt, sb, st, _ptr(cl), T, int(want_partial),
+                            _stream(stream), _ptr(words), words_cap, _ptr(wl), _ptr(sc),
+                            _ptr(meta))
+        if not want_partial:
+            return None
+        return [dict(words=words[i, : min(wl[i], words_cap)].copy(), n_words=int(wl[i]),
+                     score=float(sc[i]), ok=int(meta[i, 0]), overflow=int(meta[i, 2]))
+                for i in range(n)]
+
+    def stream_finalize(self, channels, stream=None, words_cap=4096):
+        ch = np.ascontiguousarray(channels, dtype=np.int32)
+        n = len(ch)
+        words = np.zeros((n, max(words_cap, 1)), np.int32)
+        wl = np.zeros(n, np.int32)
+        sc = np.zeros(n, np.float64)
+        meta = np.zeros((n, 3), np.int32)
+        wfst_stream_finalize(self.h, _ptr(ch), n, _stream(stream), _ptr(words), words_cap,
+                             _ptr(wl), _ptr(sc), _ptr(meta))
+        return [dict(words=words[i, : min(wl[i], words_cap)].copy(), n_words=int(wl[i]),
+                     score=float(sc[i]), ok=int(meta[i, 0]), reached_final=int(meta[i, 1]),
+                     overflow=int(meta[i, 2])) for i in range(n)]
+
+    def stream_release(self, channel: int):
+        wfst_stream_release(self.h, int(channel))
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return C.c_void_p(s)
+    return C.c_void_p(int(s.cuda_stream))   # torch.cuda.Stream

@@ -1,0 +1,161 @@
+// wfst_internal.h — device data layout shared by the host API and the
+// persistent decode kernel.  See the design notes for the memory plan.
+#pragma once
+#include <cstdint>
+
+namespace wfst {
+
+constexpr int kThreads = 512;     // threads per CTA of the persistent kernel
+constexpr int kTile = 2048;       // arc slots per work tile
+constexpr int kTokCap = 2048;     // frontier tokens staged in shared memory per tile chunk
+constexpr int kMaxLanes = 256;    // lanes per decoder
+constexpr int kWarps = kThreads / 32;
+
+// overflow bits (the page's §7 values)
+constexpr int kOvfArena = 4;
+constexpr int kOvfKept = 16;
+constexpr int kOvfPath = 32;
+
+// lattice record flags
+constexpr int kRecEps = 1;
+constexpr int kRecFinal = 2;
+constexpr int kRecRedirect = 4;
+constexpr int kRecDead = 8;       // epsilon relaxation evaluated with a non-final score
+
+// lane status
+constexpr int kLaneFree = 0;
+constexpr int kLaneRunning = 1;
+constexpr int kLaneDone = 2;
+
+// per-call lane flags
+constexpr int kCallInit = 1;      // reset the lane and open its start frontier
+constexpr int kCallFinal = 2;     // run the final step + backtrack at the end of the call
+constexpr int kCallPartial = 4;   // backtrack the best current token at the end of the call
+
+// Graph, internal layout: per state, emitting arcs first then epsilon arcs
+// (a stable partition of the caller's arcs; caller arc ids are kept).
+struct DevGraph {
+  int32_t N, start, V, has_eps;
+  int64_t A;
+  int32_t eps_depth;              // longest epsilon path (passes needed by a closure)
+  int32_t identity;               // internal arc order == caller arc order
+  const int4* meta;               // [N] {row_begin, emit_end, eps_end, emit_maxw bits}
+  const uint16_t* ilabel;         // [A] internal, 0xFFFF on epsilon arcs
+  const float* weight;            // [A] internal
+  const int32_t* dst;             // [A] internal
+  const int32_t* arc_id;          // [A] internal -> caller id (nullptr when identity)
+  const int32_t* c_src;           // [A] caller id -> src state | (epsilon << 31)
+  const int32_t* c_dst;           // [A] caller id -> dst state
+  const int32_t* c_olabel;        // [A] caller id -> olabel
+  const float* final_w;           // [N]
+};
+
+struct FrameCnt {                 // per lane, per frame (ring of 4 frames)
+  unsigned long long cnt;         // (tokens << 32) | emitting arcs of the frame's tokens
+  unsigned int maxkey;            // ordered max end of the step that consumes the frame
+  unsigned int admitted;          // admitted emitting candidates of that step
+  unsigned long long final_key;   // (ordered final score, 0x7fffffff - state)
+  unsigned long long best_key;    // (ordered score, 0x7fffffff - arc) of the best token
+};
+
+struct LaneState {                // persistent per lane (mirrored in shared memory)
+  int32_t t;                      // frames consumed; the frontier is frame t
+  int32_t committed;              // last frame whose tokens are in the winners log
+  float beam;
+  int32_t status;
+  int64_t cursor;                 // next free winners-log entry
+  int64_t base_cur;               // log base of frame `committed`
+  int64_t base_prev;              // log base of frame `committed - 1`
+  int64_t lat_cursor;             // next free lattice record
+  uint32_t eps_pass;              // epsilon worklist pass id (dedupe marks)
+  int32_t overflow;
+  int32_t t_eff;                  // offline length (last-frames rule), -1 streaming
+  int32_t pad;
+};
+
+struct LaneCall {                 // per lane, per call
+  int32_t row;                    // row of the call's log-prob tensor, -1 = not in this call
+  int32_t nframes;                // frames to consume in this call
+  int32_t flags;                  // kCall*
+  int32_t t_eff;                  // offline length, -1 streaming
+};
+
+struct LaneStats {                // per lane, accumulated by the kernel (zeroed per call)
+  unsigned long long frames, sum_n, sum_d, sum_a, sum_m, eps, finals;
+  unsigned long long steps;
+};
+
+struct LatRec {                   // 32 bytes
+  int32_t frame_flags;            // (frame << 4) | flags
+  int32_t src_tok;                // winners-log index of the source token
+  int32_t dst_tok;                // winners-log index of the destination (-1 super-final)
+  int32_t src_state;
+  int32_t dst_state;              // -1 super-final
+  int32_t arc;                    // caller arc id, or A + s
+  float end;                      // forward value of the candidate
+  float arcscore;                 // the record's own score
+};
+
+struct Result {                   // per lane, per call
+  int32_t ok, reached_final, overflow, n_words;
+  float score;
+  int32_t n_arcs;
+  int32_t pad0, pad1;
+};
+
+struct GridBar {
+  unsigned int count;             // arrivals (monotonic within a launch)
+  unsigned int abort;             // set when any wait gave up
+  unsigned int error;             // 1 = barrier timeout, 2 = closure did not converge
+  unsigned int epochs;            // barriers executed (written at the end)
+  unsigned int changed[3];        // per-pass change flags (lattice epsilon groups)
+  unsigned int pad;
+};
+
+struct DevWork {
+  int32_t L, N;
+  int64_t qcap;                   // frontier capacity per lane per frame
+  int64_t log_cap, lat_cap, path_cap;
+  int64_t tiles_cap;              // tiles per lane per frame
+  int32_t lattice, max_frames;
+  unsigned long long* payload;    // [2][L][N] recombination keys, 0 = empty
+  int32_t* tokidx;                // [2][L][N] position of a state in its frame
+  int32_t* claims;                // [2][L][qcap] states of a frame (the frontier)
+  uint32_t* arcoff;               // [2][L][qcap] emitting-arc offset of each token
+  int32_t* tile_first;            // [2][L][tiles_cap] token holding each tile's first slot
+  int32_t* wl_state;              // [2][L][qcap] epsilon worklist
+  uint32_t* wl_off;               // [2][L][qcap]
+  int32_t* wl_tile_first;         // [2][L][tiles_cap]
+  uint32_t* mark;                 // [L][N] worklist dedupe marks
+  unsigned long long* wl_cnt;     // [3][L] (tokens << 32) | epsilon arcs
+  int2* wlog;                     // [L][log_cap] {prev, arc} winners log
+  FrameCnt* fcnt;                 // [4][L]
+  LaneState* lanes;               // [L]
+  LaneStats* stats;               // [L]
+  LatRec* lat;                    // [L][lat_cap]
+  unsigned long long* lat_cnt;    // [L] records appended
+  int64_t* lat_groups;            // [L][max_frames+2] B_t: first record appended after frame t's closure
+  uint32_t* bwd;                  // [L][log_cap] ordered backward scores
+  LatRec* lat_out;                // [L][lat_cap] kept records (compacted)
+  unsigned long long* lat_out_n;  // [L]
+  int32_t* path;                  // [L][path_cap]
+  Result* res;                    // [L]
+  int32_t* words;                 // [L][words_cap] (words_cap per call)
+  GridBar* bar;
+};
+
+struct RunArgs {
+  DevGraph g;
+  DevWork w;
+  const void* lp;                 // log-prob base (device)
+  int64_t stride_b, stride_t;     // elements
+  const LaneCall* calls;          // [L] device
+  int32_t nlanes;                 // lanes scanned (max_lanes)
+  int32_t words_cap;
+  float search_beam, output_beam;
+  int32_t min_active, max_active, allow_partial, lattice;
+  int32_t nblocks;
+  int32_t ub_skip;                // upper-bound skips in the max/expand passes
+};
+
+}  // namespace wfst

@@ -1,0 +1,1222 @@
+// wfst_kernel.cu — the persistent decode kernel (sm_103a).
+//
+// One cooperative launch runs a whole decode call on the device: lane
+// initialisation, the frame-synchronous step loop, epsilon closure, the final
+// step, backtrack to words and the lattice backward prune.  Phases are
+// separated by a software grid barrier whose waits are bounded in time (an
+// expired wait aborts the launch with an error flag instead of hanging).
+//
+// Method: "GPU WFST Beam-Search Decoder" (OASR docs).  Per frame and lane:
+//   §3  dynamic beam update from the frontier size;
+//   §5.1/§5.2 the frontier's emitting arcs form one flattened slot space over
+//        all lanes, cut into fixed tiles that every CTA walks (load balance
+//        with one hot lane);
+//   §5.3 pass 1 (max): exact per-lane maximum of end = (score + w) + lp over
+//        every slot; pass 2 (expand): admit end > max - beam and recombine by
+//        destination with one 64-bit atomicMax on (ordered score, lowest arc
+//        id) — a direct-indexed per-lane table replaces the page's hash;
+//   §5.4 commit: each frontier token gets a winners-log entry {prev, arc};
+//   §5.5 epsilon closure by worklist passes to a fixpoint; lattice records;
+//   §7  backtrack from the final token; lattice backward output_beam prune.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "wfst_internal.h"
+
+namespace wfst {
+
+constexpr unsigned long long kTimeoutNs = 4000000000ull;  // 4 s per barrier wait
+
+enum Phase { kNone = 0, kEmit = 1, kFin = 2, kPart = 3 };
+
+struct SmLane {
+  int32_t t, committed, status, phase;
+  float beam, cutoff;
+  int32_t n_cur, n_prev;
+  uint32_t d_cur;
+  int32_t row, t0, t_end, flags, t_eff;
+  int32_t need_commit, done_final, done_partial, expanded;
+  int64_t cursor, base_cur, base_prev;
+  uint32_t eps_pass, wl_e;
+  int32_t wl_n, closure;
+  int64_t res_lo, res_hi;         // lattice records resolved in this step's commit phase
+  unsigned long long frames, sum_n, sum_d, sum_m;
+  int32_t was_emit, pad0;
+};
+
+struct Smem {
+  SmLane lane[kMaxLanes];
+  int32_t pre_a[kMaxLanes + 1];   // work units per lane, exclusive prefix (tiles)
+  int32_t pre_b[kMaxLanes + 1];   // commit tokens / tasks
+  int32_t pre_c[kMaxLanes + 1];   // clear tokens
+  int32_t pre_d[kMaxLanes + 1];   // lattice records to resolve
+  uint32_t tok_off[kTokCap + 1];
+  int32_t tok_row[kTokCap];
+  float tok_score[kTokCap];
+  int32_t tok_state[kTokCap];
+  float redf[kWarps];
+  uint32_t redu[kWarps];
+  int32_t scan_tmp[kWarps];
+  int32_t flag, abort, any, bt_n;
+  int64_t bt_idx;
+  int32_t bt_ok, bt_reached, bt_state, bt_pad;
+  float bt_score;
+};
+
+// ------------------------------------------------------------------ helpers
+
+__device__ __forceinline__ unsigned ord_f(float x) {
+  unsigned u = __float_as_uint(x);
+  if (u == 0x80000000u) u = 0u;  // -0 and +0 compare equal
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float unord_f(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+// (score, id): a higher score wins, then the LOWER id; id -1 (start token) is lowest.
+__device__ __forceinline__ unsigned long long mk_key(float s, int32_t id) {
+  return ((unsigned long long)ord_f(s) << 32) | (unsigned)(0x7fffffffu - (unsigned)id);
+}
+__device__ __forceinline__ int32_t key_id(unsigned long long k) {
+  return (int32_t)(0x7fffffffu - (unsigned)(k & 0xffffffffull));
+}
+__device__ __forceinline__ float key_score(unsigned long long k) { return unord_f((unsigned)(k >> 32)); }
+
+__device__ __forceinline__ unsigned long long gtimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+template <typename T>
+__device__ __forceinline__ float lp_at(const T* row, int v);
+template <>
+__device__ __forceinline__ float lp_at<float>(const float* row, int v) { return __ldg(row + v); }
+template <>
+__device__ __forceinline__ float lp_at<__half>(const __half* row, int v) {
+  return __half2float(__ldg(row + v));
+}
+
+// Largest l in [0, L) with pre[l] <= x (pre: exclusive prefix, pre[L] = total).
+__device__ __forceinline__ int find_lane(const int32_t* pre, int L, int32_t x) {
+  int lo = 0, hi = L;
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (pre[mid] <= x) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// In-place exclusive prefix of pre[0..L) (pre[L] = total), computed
+// redundantly by every CTA.  Callers synchronise before writing `pre`.
+__device__ void lane_scan(int32_t* pre, int L) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = (L + 31) / 32;
+    int32_t local = 0;
+    for (int i = 0; i < per; i++) {
+      const int idx = lane * per + i;
+      if (idx < L) local += pre[idx];
+    }
+    int32_t inc = local;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += v;
+    }
+    int32_t run = inc - local;
+    for (int i = 0; i < per; i++) {
+      const int idx = lane * per + i;
+      if (idx < L) {
+        const int32_t v = pre[idx];
+        pre[idx] = run;
+        run += v;
+      }
+    }
+    if (lane == 31) pre[L] = inc;
+  }
+  __syncthreads();
+}
+
+// Bounded software grid barrier.  Returns false when the launch aborts.
+__device__ bool grid_sync(const RunArgs& a, Smem& S, unsigned& epoch) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    GridBar* bar = a.w.bar;
+    epoch++;
+    const unsigned target = epoch * (unsigned)gridDim.x;
+    __threadfence();
+    atomicAdd(&bar->count, 1u);
+    int ab = 0;
+    const unsigned long long t0 = gtimer();
+    for (;;) {
+      const unsigned c = ld_acquire(&bar->count);
+      if ((int)(c - target) >= 0) break;
+      if (ld_acquire(&bar->abort)) { ab = 1; break; }
+      if (gtimer() - t0 > kTimeoutNs) {
+        atomicExch(&bar->abort, 1u);
+        atomicOr(&bar->error, 1u);
+        ab = 1;
+        break;
+      }
+      __nanosleep(32);
+    }
+    __threadfence();
+    S.abort = ab;
+  }
+  __syncthreads();
+  return S.abort == 0;
+}
+
+__device__ __forceinline__ float block_max_f(float v, Smem& S) {
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) S.redf[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = S.redf[0];
+  for (int i = 1; i < kWarps; i++) r = fmaxf(r, S.redf[i]);
+  return r;
+}
+__device__ __forceinline__ uint32_t block_sum_u(uint32_t v, Smem& S) {
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) S.redu[threadIdx.x >> 5] = v;
+  __syncthreads();
+  uint32_t r = 0;
+  for (int i = 0; i < kWarps; i++) r += S.redu[i];
+  return r;
+}
+
+__device__ __forceinline__ void lane_ovf(const RunArgs& a, int l, int bits) {
+  atomicOr(&a.w.lanes[l].overflow, bits);
+}
+
+__device__ __forceinline__ size_t pl(const DevWork& w, int par, int l) {
+  return ((size_t)par * w.L + l) * (size_t)w.N;       // payload / tokidx row
+}
+__device__ __forceinline__ size_t ql(const DevWork& w, int par, int l) {
+  return ((size_t)par * w.L + l) * (size_t)w.qcap;    // claims / arcoff / worklists
+}
+__device__ __forceinline__ size_t tl(const DevWork& w, int par, int l) {
+  return ((size_t)par * w.L + l) * (size_t)w.tiles_cap;
+}
+__device__ __forceinline__ FrameCnt* fc_of(const DevWork& w, int f, int l) {
+  return w.fcnt + (size_t)(f & 3) * w.L + l;
+}
+
+// Warp-wide exclusive scan helper: returns the inclusive prefix of v.
+__device__ __forceinline__ uint32_t warp_inc_scan(uint32_t v) {
+  const int lane = threadIdx.x & 31;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += x;
+  }
+  return v;
+}
+
+// Warp-cooperative append of states to a frontier-like list: one 64-bit
+// atomic per warp returns both the positions and an exclusive prefix of the
+// per-state arc counts (so each token gets a contiguous arc-slot range), and
+// every tile boundary that falls inside a token's range records that token.
+__device__ __forceinline__ void warp_list_append(bool want, int32_t d, uint32_t deg,
+                                                 unsigned long long* ctr, int32_t* states,
+                                                 uint32_t* offs, int32_t* tfirst, int32_t* tokidx,
+                                                 int64_t cap, const RunArgs& a, int l) {
+  const unsigned full = 0xffffffffu;
+  const unsigned m = __ballot_sync(full, want);
+  if (!m) return;
+  const int lane = threadIdx.x & 31;
+  const uint32_t dv = want ? deg : 0u;
+  const uint32_t inc = warp_inc_scan(dv);
+  const uint32_t total = __shfl_sync(full, inc, 31);
+  const int leader = __ffs(m) - 1;
+  unsigned long long base = 0;
+  if (lane == leader) base = atomicAdd(ctr, ((unsigned long long)__popc(m) << 32) | total);
+  base = __shfl_sync(full, base, leader);
+  if (want) {
+    const uint32_t p = (uint32_t)(base >> 32) + __popc(m & lanemask_lt());
+    const uint32_t off = (uint32_t)base + inc - dv;
+    if (p < (uint64_t)cap) {
+      states[p] = d;
+      offs[p] = off;
+      if (tokidx) tokidx[d] = (int32_t)p;
+      if (dv > 0) {
+        const uint32_t k0 = (off + kTile - 1) / kTile, k1 = (off + dv - 1) / kTile;
+        for (uint32_t k = k0; k <= k1; k++) tfirst[k] = (int32_t)p;
+      }
+    } else {
+      lane_ovf(a, l, kOvfKept);
+    }
+  }
+}
+
+// Claim states into frame f of lane l (and seed the epsilon worklist W0).
+__device__ __forceinline__ void warp_claim(const RunArgs& a, bool want, int32_t d, int l, int f,
+                                           bool seed_worklist) {
+  const DevWork& w = a.w;
+  const unsigned m = __ballot_sync(0xffffffffu, want);
+  if (!m) return;
+  int4 meta = make_int4(0, 0, 0, 0);
+  if (want) meta = __ldg(a.g.meta + d);
+  const int par = f & 1;
+  warp_list_append(want, d, (uint32_t)(meta.y - meta.x), &fc_of(w, f, l)->cnt,
+                   w.claims + ql(w, par, l), w.arcoff + ql(w, par, l), w.tile_first + tl(w, par, l),
+                   w.tokidx + pl(w, par, l), w.qcap, a, l);
+  if (a.g.has_eps && seed_worklist) {
+    const bool ws = want && (meta.z > meta.y);
+    warp_list_append(ws, d, (uint32_t)(meta.z - meta.y), &w.wl_cnt[l], w.wl_state + ql(w, 0, l),
+                     w.wl_off + ql(w, 0, l), w.wl_tile_first + tl(w, 0, l), nullptr, w.qcap, a, l);
+  }
+}
+
+// Warp-cooperative lattice record append.
+__device__ __forceinline__ void warp_lat_append(const RunArgs& a, bool want, int l, const LatRec& r) {
+  const DevWork& w = a.w;
+  const unsigned full = 0xffffffffu;
+  const unsigned m = __ballot_sync(full, want);
+  if (!m) return;
+  const int lane = threadIdx.x & 31;
+  const int ld = __ffs(m) - 1;
+  unsigned long long b = 0;
+  if (lane == ld) b = atomicAdd(&w.lat_cnt[l], (unsigned long long)__popc(m));
+  b = __shfl_sync(full, b, ld);
+  if (want) {
+    const unsigned long long p = b + __popc(m & lanemask_lt());
+    if (p < (unsigned long long)w.lat_cap) w.lat[(size_t)l * w.lat_cap + p] = r;
+    else lane_ovf(a, l, kOvfArena);
+  }
+}
+
+// ------------------------------------------------------------------ emitting tiles
+
+// MODE 0: exact per-lane max of end over the frame's emitting arcs.
+// MODE 1: admission against the cutoff + recombination into the next frame.
+template <int MODE, typename LP>
+__device__ void emit_tiles(const RunArgs& a, Smem& S) {
+  const DevWork& w = a.w;
+  const DevGraph& g = a.g;
+  const int L = a.nlanes;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int total = S.pre_a[L];
+  const LP* lpb = reinterpret_cast<const LP*>(a.lp);
+  for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    const int l = find_lane(S.pre_a, L, tile);
+    const int k = tile - S.pre_a[l];
+    const SmLane& s = S.lane[l];
+    const int f = s.t, par = f & 1;
+    const int ntiles = S.pre_a[l + 1] - S.pre_a[l];
+    const uint32_t s_lo = (uint32_t)k * kTile;
+    const uint32_t s_hi = min(s_lo + (uint32_t)kTile, s.d_cur);
+    const int32_t p_lo = __ldcg(w.tile_first + tl(w, par, l) + k);
+    int32_t p_hi = (k + 1 < ntiles) ? __ldcg(w.tile_first + tl(w, par, l) + k + 1) + 1 : s.n_cur;
+    if (p_hi > s.n_cur) p_hi = s.n_cur;
+    const LP* row = lpb + (int64_t)s.row * a.stride_b + (int64_t)(f - s.t0) * a.stride_t;
+    const float cutoff = s.cutoff;
+    const size_t q = ql(w, par, l);
+    const size_t pay = pl(w, par, l);
+    const size_t npay = pl(w, par ^ 1, l);
+    float vmax = -INFINITY;
+    uint32_t admitted = 0;
+    for (int32_t c = p_lo; c < p_hi; c += kTokCap) {
+      const int ntok = min(kTokCap, p_hi - c);
+      __syncthreads();
+      for (int i = tid; i < ntok; i += kThreads) {
+        const int32_t p = c + i;
+        const int32_t d = __ldcg(w.claims + q + p);
+        S.tok_off[i] = __ldcg(w.arcoff + q + p);
+        S.tok_row[i] = __ldg(&g.meta[d].x);
+        S.tok_score[i] = key_score(__ldcg(w.payload + pay + d));
+        S.tok_state[i] = d;
+      }
+      if (tid == 0) S.tok_off[ntok] = (c + ntok < s.n_cur) ? __ldcg(w.arcoff + q + c + ntok) : s.d_cur;
+      __syncthreads();
+      const uint32_t c_lo = max(s_lo, S.tok_off[0]);
+      const uint32_t c_hi = min(s_hi, S.tok_off[ntok]);
+      for (uint32_t base = c_lo + warp * 32; base < c_hi; base += kThreads) {
+        const uint32_t slot = base + lane;
+        const bool valid = slot < c_hi;
+        float end = -INFINITY, arcsc = 0.f;
+        int32_t ai = 0, i = 0;
+        if (valid) {
+          int lo = 0, hi = ntok;  // largest i with tok_off[i] <= slot
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (S.tok_off[mid] <= slot) lo = mid; else hi = mid;
+          }
+          i = lo;
+          ai = S.tok_row[i] + (int32_t)(slot - S.tok_off[i]);
+          const int il = __ldg(g.ilabel + ai);
+          const float wt = __ldg(g.weight + ai);
+          const float lpv = lp_at<LP>(row, il);
+          end = __fadd_rn(__fadd_rn(S.tok_score[i], wt), lpv);
+          arcsc = __fadd_rn(wt, lpv);
+        }
+        if (MODE == 0) {
+          vmax = fmaxf(vmax, end);
+        } else {
+          const bool adm = valid && (end > cutoff);
+          bool claim = false;
+          int32_t d = 0, id = 0;
+          if (adm) {
+            admitted++;
+            d = __ldg(g.dst + ai);
+            id = g.identity ? ai : __ldg(g.arc_id + ai);
+            const unsigned long long old = atomicMax(w.payload + npay + d, mk_key(end, id));
+            claim = (old == 0ull);
+          }
+          warp_claim(a, claim, d, l, f + 1, true);
+          if (a.lattice) {
+            LatRec r;
+            r.frame_flags = f << 4;
+            r.src_tok = (int32_t)(s.base_cur + (c + i));
+            r.dst_tok = -1;
+            r.src_state = S.tok_state[i];
+            r.dst_state = d;
+            r.arc = id;
+            r.end = end;
+            r.arcscore = arcsc;
+            warp_lat_append(a, adm, l, r);
+          }
+        }
+      }
+    }
+    if (MODE == 0) {
+      const float bm = block_max_f(vmax, S);
+      if (tid == 0) atomicMax(&fc_of(w, f, l)->maxkey, ord_f(bm));
+    } else {
+      const uint32_t ad = block_sum_u(admitted, S);
+      if (tid == 0 && ad) atomicAdd(&w.stats[l].sum_a, (unsigned long long)ad);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ epsilon closure
+
+// Relax the epsilon arcs of worklist `buf` (each closure lane's frame);
+// improved or new states with epsilon arcs go to worklist buf^1, count slot
+// `next_slot`, deduplicated by this pass's mark.
+__device__ void eps_tiles(const RunArgs& a, Smem& S, int buf, int next_slot) {
+  const DevWork& w = a.w;
+  const DevGraph& g = a.g;
+  const int L = a.nlanes;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int total = S.pre_a[L];
+  for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    const int l = find_lane(S.pre_a, L, tile);
+    const int k = tile - S.pre_a[l];
+    const SmLane& s = S.lane[l];
+    const int f = s.closure;        // closure frame + 1
+    const int fr = f - 1;
+    const int par = fr & 1;
+    const int ntiles = S.pre_a[l + 1] - S.pre_a[l];
+    const uint32_t s_lo = (uint32_t)k * kTile;
+    const uint32_t s_hi = min(s_lo + (uint32_t)kTile, s.wl_e);
+    const int32_t p_lo = __ldcg(w.wl_tile_first + tl(w, buf, l) + k);
+    int32_t p_hi = (k + 1 < ntiles) ? __ldcg(w.wl_tile_first + tl(w, buf, l) + k + 1) + 1 : s.wl_n;
+    if (p_hi > s.wl_n) p_hi = s.wl_n;
+    const float cutoff = s.cutoff;
+    const size_t q = ql(w, buf, l);
+    const size_t pay = pl(w, par, l);
+    const uint32_t pass_id = s.eps_pass + 1;
+    for (int32_t c = p_lo; c < p_hi; c += kTokCap) {
+      const int ntok = min(kTokCap, p_hi - c);
+      __syncthreads();
+      for (int i = tid; i < ntok; i += kThreads) {
+        const int32_t p = c + i;
+        const int32_t u = __ldcg(w.wl_state + q + p);
+        S.tok_off[i] = __ldcg(w.wl_off + q + p);
+        S.tok_row[i] = __ldg(&g.meta[u].y);  // first epsilon arc
+        S.tok_score[i] = key_score(__ldcg(w.payload + pay + u));
+        S.tok_state[i] = u;
+      }
+      if (tid == 0) S.tok_off[ntok] = (c + ntok < s.wl_n) ? __ldcg(w.wl_off + q + c + ntok) : s.wl_e;
+      __syncthreads();
+      const uint32_t c_lo = max(s_lo, S.tok_off[0]);
+      const uint32_t c_hi = min(s_hi, S.tok_off[ntok]);
+      for (uint32_t base = c_lo + warp * 32; base < c_hi; base += kThreads) {
+        const uint32_t slot = base + lane;
+        const bool valid = slot < c_hi;
+        bool adm = false, claim = false, wl = false;
+        int32_t d = 0, id = 0, i = 0;
+        float e = 0.f, wt = 0.f;
+        uint32_t edeg = 0;
+        if (valid) {
+          int lo = 0, hi = ntok;
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (S.tok_off[mid] <= slot) lo = mid; else hi = mid;
+          }
+          i = lo;
+          const int32_t ai = S.tok_row[i] + (int32_t)(slot - S.tok_off[i]);
+          wt = __ldg(g.weight + ai);
+          e = __fadd_rn(S.tok_score[i], wt);
+          if (e > cutoff) {
+            adm = true;
+            d = __ldg(g.dst + ai);
+            id = g.identity ? ai : __ldg(g.arc_id + ai);
+            const unsigned long long key = mk_key(e, id);
+            const unsigned long long old = atomicMax(w.payload + pay + d, key);
+            claim = (old == 0ull);
+            if (key > old) {
+              const int4 md = __ldg(g.meta + d);
+              if (md.z > md.y) {
+                const uint32_t prevmark = atomicExch(w.mark + (size_t)l * w.N + d, pass_id);
+                wl = (prevmark != pass_id);
+                edeg = (uint32_t)(md.z - md.y);
+              }
+            }
+          }
+        }
+        warp_claim(a, claim, d, l, fr, false);
+        warp_list_append(wl, d, edeg, &w.wl_cnt[(size_t)next_slot * L + l], w.wl_state + ql(w, buf ^ 1, l),
+                         w.wl_off + ql(w, buf ^ 1, l), w.wl_tile_first + tl(w, buf ^ 1, l), nullptr,
+                         w.qcap, a, l);
+        if (a.lattice) {
+          LatRec r;
+          r.frame_flags = (fr << 4) | kRecEps;
+          r.src_tok = __float_as_int(S.tok_score[i]);  // score used; checked at resolution
+          r.dst_tok = -1;
+          r.src_state = S.tok_state[i];
+          r.dst_state = d;
+          r.arc = id;
+          r.end = e;
+          r.arcscore = wt;
+          warp_lat_append(a, adm, l, r);
+        }
+      }
+    }
+  }
+}
+
+// Closure, to a fixpoint, of frame (s.closure - 1) of every lane with
+// s.closure > 0, against s.cutoff.  Worklist W0 is in buffer 0 / count slot 0.
+__device__ bool run_closure(const RunArgs& a, Smem& S, unsigned& epoch) {
+  const DevWork& w = a.w;
+  const int L = a.nlanes;
+  const int tid = threadIdx.x;
+  for (int k = 0;; k++) {
+    const int buf = k & 1, slot = k % 3, next_slot = (k + 1) % 3, zero_slot = (k + 2) % 3;
+    for (int l = tid; l < L; l += kThreads) {
+      SmLane& s = S.lane[l];
+      S.pre_a[l] = 0;
+      if (s.closure) {
+        const unsigned long long c = __ldcg(w.wl_cnt + (size_t)slot * L + l);
+        if ((c >> 32) > (unsigned long long)w.qcap) {
+          s.wl_n = 0;  // the worklist overflowed (lane already flagged)
+          s.wl_e = 0;
+        } else {
+          s.wl_n = (int32_t)(c >> 32);
+          s.wl_e = (uint32_t)c;
+        }
+        S.pre_a[l] = (int32_t)((s.wl_e + kTile - 1) / kTile);
+      }
+    }
+    __syncthreads();
+    lane_scan(S.pre_a, L);
+    if (S.pre_a[L] == 0) break;
+    if (k > a.g.eps_depth + 2) {  // cannot happen on an acyclic epsilon subgraph
+      if (tid == 0 && blockIdx.x == 0) atomicOr(&w.bar->error, 2u);
+      break;
+    }
+    if (blockIdx.x == 0)
+      for (int l = tid; l < L; l += kThreads)
+        if (S.lane[l].closure) w.wl_cnt[(size_t)zero_slot * L + l] = 0ull;
+    eps_tiles(a, S, buf, next_slot);
+    __syncthreads();
+    for (int l = tid; l < L; l += kThreads)
+      if (S.lane[l].closure) S.lane[l].eps_pass += 1;
+    if (!grid_sync(a, S, epoch)) return false;
+  }
+  for (int l = tid; l < L; l += kThreads)
+    if (S.lane[l].closure) S.lane[l].eps_pass += 1;
+  __syncthreads();
+  return true;
+}
+
+// ------------------------------------------------------------------ lane setup
+
+__device__ void init_lane_global(const RunArgs& a, int l) {
+  const DevWork& w = a.w;
+  const DevGraph& g = a.g;
+  FrameCnt z;
+  z.cnt = 0; z.maxkey = 0; z.admitted = 0; z.final_key = 0; z.best_key = 0;
+  for (int r = 0; r < 4; r++) w.fcnt[(size_t)r * w.L + l] = z;
+  for (int r = 0; r < 3; r++) w.wl_cnt[(size_t)r * w.L + l] = 0ull;
+  if (w.lattice) {
+    w.lat_cnt[l] = 0ull;
+    w.lat_out_n[l] = 0ull;
+  }
+  w.lanes[l].overflow = 0;
+  const int32_t s0 = g.start;
+  const int4 m = __ldg(g.meta + s0);
+  const uint32_t deg = (uint32_t)(m.y - m.x);
+  w.payload[pl(w, 0, l) + s0] = mk_key(0.0f, -1);
+  w.claims[ql(w, 0, l)] = s0;
+  w.arcoff[ql(w, 0, l)] = 0u;
+  w.tokidx[pl(w, 0, l) + s0] = 0;
+  if (deg > 0)
+    for (uint32_t k = 0; k <= (deg - 1) / kTile; k++) w.tile_first[tl(w, 0, l) + k] = 0;
+  w.fcnt[l].cnt = (1ull << 32) | deg;
+  if (g.has_eps && m.z > m.y) {
+    const uint32_t edeg = (uint32_t)(m.z - m.y);
+    w.wl_state[ql(w, 0, l)] = s0;
+    w.wl_off[ql(w, 0, l)] = 0u;
+    for (uint32_t k = 0; k <= (edeg - 1) / kTile; k++) w.wl_tile_first[tl(w, 0, l) + k] = 0;
+    w.wl_cnt[l] = (1ull << 32) | edeg;
+  }
+}
+
+// ------------------------------------------------------------------ lattice prune
+
+// Backward scores over the persisted records of every lane with s.closure
+// set, in reverse append order, then the keep test (§3: output_beam acts only
+// here) and compaction of the kept records.
+//   Append order per lane: R_{-1} = eps(0), then for t = 0..T-1
+//   R_t = emit(t) + eps(t+1), then R_T = final(T) (+ redirect).  B_t (the
+//   start of R_t) is recorded in lat_groups during frame t's commit phase.
+//   Backward group j: j = 0 -> R_T; j odd -> epsilon records of R_{T-1-(j-1)/2};
+//   j even (> 0) -> emitting records of R_{T-1-(j-2)/2}.
+__device__ bool lattice_prune(const RunArgs& a, Smem& S, unsigned& epoch) {
+  const DevWork& w = a.w;
+  const DevGraph& g = a.g;
+  const int L = a.nlanes;
+  const int tid = threadIdx.x;
+  const int G = gridDim.x;
+  const int64_t gstride = (int64_t)G * kThreads;
+  const int64_t gstart = (int64_t)blockIdx.x * kThreads + tid;
+  for (int l = 0; l < L; l++) {
+    const SmLane& s = S.lane[l];
+    if (!s.closure) continue;
+    const int64_t n = min(s.cursor, w.log_cap);
+    uint32_t* bw = w.bwd + (size_t)l * w.log_cap;
+    for (int64_t i = gstart; i < n; i += gstride) bw[i] = ord_f(-INFINITY);
+  }
+  if (blockIdx.x == 0 && tid < 3) w.bar->changed[tid] = 0u;
+  if (!grid_sync(a, S, epoch)) return false;
+  int maxg = 0;
+  for (int l = 0; l < L; l++)
+    if (S.lane[l].closure) maxg = max(maxg, 2 * S.lane[l].t + 2);
+  int pass_no = 0;
+  for (int j = 0; j < maxg; j++) {
+    const bool eps_group = (j & 1) == 1;
+    if (eps_group && !g.has_eps) continue;
+    const int npass = eps_group ? g.eps_depth + 2 : 1;
+    for (int pass = 0; pass < npass; pass++, pass_no++) {
+      const int fl = pass_no % 3;
+      if (blockIdx.x == 0 && tid == 0) w.bar->changed[(pass_no + 1) % 3] = 0u;
+      for (int l = 0; l < L; l++) {
+        const SmLane& s = S.lane[l];
+        if (!s.closure) continue;
+        const int T = s.t;
+        const int64_t* B = w.lat_groups + (size_t)l * (w.max_frames + 2);
+        const int64_t total = (int64_t)min(__ldcg(&w.lat_cnt[l]), (unsigned long long)w.lat_cap);
+        int64_t lo, hi;
+        if (j == 0) {
+          lo = B[T];
+          hi = total;
+        } else {
+          const int r = T - 1 - (j - 1) / 2;  // R_r, r >= -1
+          if (r < -1) continue;
+          lo = (r < 0) ? 0 : B[r];
+          hi = B[r + 1];
+        }
+        const LatRec* R = w.lat + (size_t)l * w.lat_cap;
+        uint32_t* bw = w.bwd + (size_t)l * w.log_cap;
+        for (int64_t r = lo + gstart; r < hi; r += gstride) {
+          const LatRec rec = R[r];
+          const int flags = rec.frame_flags & 15;
+          if (flags & kRecDead) continue;
+          if (j > 0 && (((flags & kRecEps) != 0) != eps_group)) continue;
+          const float bd = rec.dst_tok < 0 ? 0.0f : unord_f(__ldcg(bw + rec.dst_tok));
+          const unsigned ov = ord_f(__fadd_rn(rec.arcscore, bd));
+          const unsigned old = atomicMax(bw + rec.src_tok, ov);
+          if (eps_group && ov > old) w.bar->changed[fl] = 1u;
+        }
+      }
+      if (!grid_sync(a, S, epoch)) return false;
+      if (eps_group && ld_acquire(&w.bar->changed[fl]) == 0u) break;
+    }
+  }
+  // keep test and compaction
+  const int lane = tid & 31;
+  for (int l = 0; l < L; l++) {
+    const SmLane& s = S.lane[l];
+    if (!s.closure) continue;
+    const float thr = __fsub_rn(__ldcg(&w.res[l].score), a.output_beam);
+    const int64_t hi = (int64_t)min(__ldcg(&w.lat_cnt[l]), (unsigned long long)w.lat_cap);
+    const LatRec* R = w.lat + (size_t)l * w.lat_cap;
+    const uint32_t* bw = w.bwd + (size_t)l * w.log_cap;
+    for (int64_t base = (int64_t)blockIdx.x * kThreads + (tid & ~31); base < hi; base += gstride) {
+      const int64_t r = base + lane;
+      bool keep = false;
+      LatRec rec;
+      if (r < hi) {
+        rec = R[r];
+        if (!(rec.frame_flags & kRecDead)) {
+          const float bd = rec.dst_tok < 0 ? 0.0f : unord_f(__ldcg(bw + rec.dst_tok));
+          keep = __fadd_rn(rec.end, bd) >= thr;
+        }
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, keep);
+      if (m) {
+        const int ld = __ffs(m) - 1;
+        unsigned long long b = 0;
+        if (lane == ld) b = atomicAdd(&w.lat_out_n[l], (unsigned long long)__popc(m));
+        b = __shfl_sync(0xffffffffu, b, ld);
+        if (keep) w.lat_out[(size_t)l * w.lat_cap + b + __popc(m & lanemask_lt())] = rec;
+      }
+    }
+  }
+  return true;
+}
+
+// ------------------------------------------------------------------ the kernel
+
+template <typename LP>
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Smem& S = *reinterpret_cast<Smem*>(smem_raw);
+  const DevWork& w = a.w;
+  const DevGraph& g = a.g;
+  const int L = a.nlanes;
+  const int tid = threadIdx.x;
+  const int G = gridDim.x;
+  const int64_t gstride = (int64_t)G * kThreads;
+  const int64_t gstart = (int64_t)blockIdx.x * kThreads + tid;
+  const bool lat = a.lattice != 0;
+  unsigned epoch = 0;
+  unsigned long long steps = 0;
+
+  // ---- lane mirrors (every CTA holds an identical copy)
+  for (int l = tid; l < L; l += kThreads) {
+    SmLane& s = S.lane[l];
+    const LaneState st = w.lanes[l];
+    const LaneCall c = a.calls[l];
+    s.t = st.t;
+    s.committed = st.committed;
+    s.status = st.status;
+    s.beam = st.beam;
+    s.cursor = st.cursor;
+    s.base_cur = st.base_cur;
+    s.base_prev = st.base_prev;
+    s.eps_pass = st.eps_pass;
+    s.t_eff = st.t_eff;
+    s.row = c.row;
+    s.flags = c.row >= 0 ? c.flags : 0;
+    s.phase = kNone;
+    s.done_final = s.done_partial = 0;
+    s.frames = s.sum_n = s.sum_d = s.sum_m = 0;
+    s.was_emit = 0;
+    s.closure = 0;
+    s.cutoff = 0.f;
+    s.n_cur = s.n_prev = 0;
+    s.d_cur = 0;
+    if (s.flags & kCallInit) {
+      s.t = 0;
+      s.committed = -1;
+      s.status = kLaneRunning;
+      s.beam = a.search_beam;
+      s.cursor = s.base_cur = s.base_prev = 0;
+      s.t_eff = c.t_eff;
+    }
+    s.t0 = s.t;
+    s.t_end = s.t + (c.row >= 0 ? c.nframes : 0);
+  }
+  __syncthreads();
+
+  // ---- lane initialisation + start-frontier closure (cutoff 0 - search_beam)
+  if (tid == 0) {
+    int any = 0;
+    for (int l = 0; l < L; l++) any |= (S.lane[l].flags & kCallInit);
+    S.any = any;
+  }
+  __syncthreads();
+  if (S.any) {
+    if (tid == 0)
+      for (int l = blockIdx.x; l < L; l += G)
+        if (S.lane[l].flags & kCallInit) init_lane_global(a, l);
+    if (!grid_sync(a, S, epoch)) return;
+    if (g.has_eps) {
+      for (int l = tid; l < L; l += kThreads) {
+        SmLane& s = S.lane[l];
+        s.closure = (s.flags & kCallInit) ? 1 : 0;  // frame 0
+        s.cutoff = __fsub_rn(0.0f, a.search_beam);
+      }
+      __syncthreads();
+      if (!run_closure(a, S, epoch)) return;
+      for (int l = tid; l < L; l += kThreads) S.lane[l].closure = 0;
+      __syncthreads();
+    }
+  }
+
+  // ---- the frame loop
+  for (;;) {
+    // prologue: each lane's phase and frame sizes (identical in every CTA;
+    // the counters it reads are final since the last barrier)
+    for (int l = tid; l < L; l += kThreads) {
+      SmLane& s = S.lane[l];
+      s.phase = kNone;
+      s.need_commit = 0;
+      S.pre_a[l] = S.pre_b[l] = S.pre_c[l] = S.pre_d[l] = 0;
+      s.res_lo = s.res_hi = 0;
+      if (s.row < 0 || s.status != kLaneRunning) continue;
+      if (s.was_emit) s.sum_m += __ldcg(&fc_of(w, s.t, l)->cnt) >> 32;
+      s.was_emit = 0;
+      if (s.t < s.t_end) s.phase = kEmit;
+      else if ((s.flags & kCallFinal) && !s.done_final) s.phase = kFin;
+      else if ((s.flags & kCallPartial) && !(s.flags & kCallFinal) && !s.done_partial) s.phase = kPart;
+      if (s.phase == kNone) continue;
+      const unsigned long long cnt = __ldcg(&fc_of(w, s.t, l)->cnt);
+      const unsigned long long n_raw = cnt >> 32;
+      s.n_cur = (int32_t)min(n_raw, (unsigned long long)w.qcap);
+      s.d_cur = (uint32_t)cnt;
+      if (n_raw > (unsigned long long)w.qcap) {
+        // tokens past the capacity were dropped: their slots are the tail
+        const size_t q = ql(w, s.t & 1, l);
+        const int32_t lastd = __ldcg(w.claims + q + s.n_cur - 1);
+        const int4 m = __ldg(g.meta + lastd);
+        s.d_cur = __ldcg(w.arcoff + q + s.n_cur - 1) + (uint32_t)(m.y - m.x);
+      }
+      s.n_prev = 0;
+      if (s.t >= 1 && s.phase != kPart) {
+        const unsigned long long cp = __ldcg(&fc_of(w, s.t - 1, l)->cnt);
+        s.n_prev = (int32_t)min(cp >> 32, (unsigned long long)w.qcap);
+      }
+      s.need_commit = (s.committed < s.t) ? 1 : 0;
+      if (s.phase == kEmit) {
+        // dynamic beam (§3 "Dynamic beam")
+        int32_t min_a = a.min_active;
+        if (s.t_eff >= 0 && s.t >= s.t_eff - 5) min_a = max(min_a, a.max_active / 2);
+        const int64_t n = (int64_t)n_raw;
+        const float sb = a.search_beam;
+        float b = s.beam;
+        if (n == 0 || ((int64_t)min_a <= n && n <= (int64_t)a.max_active))
+          b = __fadd_rn(__fmul_rn(0.8f, b), __fmul_rn(0.2f, sb));
+        else if (n < (int64_t)min_a)
+          b = __fmul_rn(fmaxf(b, sb), 1.25f);
+        else
+          b = __fmul_rn(fminf(b, sb), 0.8f);
+        s.beam = b;
+        S.pre_a[l] = (int32_t)((s.d_cur + kTile - 1) / kTile);
+        s.frames += 1;
+        s.sum_n += n_raw;
+        s.sum_d += s.d_cur;
+      }
+      S.pre_b[l] = (s.need_commit || s.phase == kFin || s.phase == kPart) ? s.n_cur : 0;
+      S.pre_c[l] = s.n_prev;
+      if (lat && s.need_commit) {
+        // records appended since frame t-1's commit: emit(t-1) and eps(t)
+        // (for t = 0: the start closure's records)
+        const int64_t* B = w.lat_groups + (size_t)l * (w.max_frames + 2);
+        s.res_lo = (s.t >= 1) ? B[s.t - 1] : 0;
+        s.res_hi = (int64_t)min(__ldcg(&w.lat_cnt[l]), (unsigned long long)w.lat_cap);
+        S.pre_d[l] = (int32_t)(s.res_hi - s.res_lo);
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int any = 0;
+      for (int l = 0; l < L; l++) any |= S.lane[l].phase;
+      S.any = any;
+    }
+    __syncthreads();
+    if (!S.any) break;
+    steps++;
+    lane_scan(S.pre_a, L);
+    lane_scan(S.pre_b, L);
+    lane_scan(S.pre_c, L);
+    lane_scan(S.pre_d, L);
+
+    // ================= phase X: commit frame t, clear frame t-1, exact max
+    if (blockIdx.x == 0) {
+      for (int l = tid; l < L; l += kThreads) {
+        const SmLane& s = S.lane[l];
+        if (s.phase == kEmit) {
+          FrameCnt z;
+          z.cnt = 0; z.maxkey = 0; z.admitted = 0; z.final_key = 0; z.best_key = 0;
+          *fc_of(w, s.t + 1, l) = z;
+          if (g.has_eps) w.wl_cnt[l] = 0ull;
+        }
+        if (lat && s.phase != kNone && s.need_commit)
+          w.lat_groups[(size_t)l * (w.max_frames + 2) + s.t] = s.res_hi;
+      }
+    }
+    {  // commit (§5.4): winners-log entry {prev, arc} per token; final-step keys
+      const int total = S.pre_b[L];
+      for (int gi = (int)gstart; gi < total; gi += (int)gstride) {
+        const int l = find_lane(S.pre_b, L, gi);
+        const int32_t p = gi - S.pre_b[l];
+        const SmLane& s = S.lane[l];
+        const int f = s.t, par = f & 1;
+        const int32_t d = __ldcg(w.claims + ql(w, par, l) + p);
+        const unsigned long long key = __ldcg(w.payload + pl(w, par, l) + d);
+        const int32_t arc = key_id(key);
+        const float score = key_score(key);
+        if (s.need_commit) {
+          const int64_t base_new = s.cursor;   // frame f
+          const int64_t base_old = s.base_cur; // frame f-1
+          int32_t prev = -1;
+          if (arc >= 0) {
+            const int32_t se = __ldg(g.c_src + arc);
+            const int32_t src = se & 0x7fffffff;
+            if (se < 0) prev = (int32_t)(base_new + __ldcg(w.tokidx + pl(w, par, l) + src));
+            else prev = (int32_t)(base_old + __ldcg(w.tokidx + pl(w, par ^ 1, l) + src));
+          }
+          const int64_t idx = base_new + p;
+          if (idx < w.log_cap) w.wlog[(size_t)l * w.log_cap + idx] = make_int2(prev, arc);
+          else lane_ovf(a, l, kOvfArena);
+          if (g.has_eps) {
+            const int4 m = __ldg(g.meta + d);
+            if (m.z > m.y) atomicAdd(&w.stats[l].eps, (unsigned long long)(m.z - m.y));
+          }
+        }
+        if (s.phase == kFin) {
+          const float fw = __ldg(g.final_w + d);
+          if (fw > -INFINITY) {
+            atomicMax(&fc_of(w, f, l)->final_key, mk_key(__fadd_rn(score, fw), d));
+            atomicAdd(&w.stats[l].finals, 1ull);
+          }
+        }
+        if (s.phase == kFin || s.phase == kPart) atomicMax(&fc_of(w, f, l)->best_key, key);
+      }
+    }
+    {  // clear frame t-1's recombination entries
+      const int total = S.pre_c[L];
+      for (int gi = (int)gstart; gi < total; gi += (int)gstride) {
+        const int l = find_lane(S.pre_c, L, gi);
+        const int32_t p = gi - S.pre_c[l];
+        const int par = (S.lane[l].t - 1) & 1;
+        const int32_t d = __ldcg(w.claims + ql(w, par, l) + p);
+        w.payload[pl(w, par, l) + d] = 0ull;
+      }
+    }
+    if (lat) {  // lattice records of the last step: resolve their frame-t tokens
+      const int total = S.pre_d[L];
+      for (int gi = (int)gstart; gi < total; gi += (int)gstride) {
+        const int l = find_lane(S.pre_d, L, gi);
+        const SmLane& s = S.lane[l];
+        const int64_t r = s.res_lo + (gi - S.pre_d[l]);
+        LatRec* rp = w.lat + (size_t)l * w.lat_cap + r;
+        LatRec rec = *rp;
+        const int par = s.t & 1;
+        const int64_t base_new = s.cursor;  // frame t
+        rec.dst_tok = (int32_t)(base_new + __ldcg(w.tokidx + pl(w, par, l) + rec.dst_state));
+        if (rec.frame_flags & kRecEps) {
+          // keep only the relaxation evaluated with the source's final score
+          const unsigned used = (unsigned)rec.src_tok;
+          const float fin = key_score(__ldcg(w.payload + pl(w, par, l) + rec.src_state));
+          rec.src_tok = (int32_t)(base_new + __ldcg(w.tokidx + pl(w, par, l) + rec.src_state));
+          if (ord_f(__uint_as_float(used)) != ord_f(fin)) rec.frame_flags |= kRecDead;
+        }
+        *rp = rec;
+      }
+    }
+    emit_tiles<0, LP>(a, S);
+    if (!grid_sync(a, S, epoch)) return;
+
+    // ================= phase Y: expand (admit + recombine); final / partial
+    for (int l = tid; l < L; l += kThreads) {
+      SmLane& s = S.lane[l];
+      S.pre_a[l] = 0;
+      if (s.phase == kNone) continue;
+      if (s.need_commit) {
+        s.base_prev = s.base_cur;
+        s.base_cur = s.cursor;
+        s.cursor += s.n_cur;
+        s.committed = s.t;
+      }
+      s.expanded = 0;
+      if (s.phase == kEmit) {
+        const unsigned mk = __ldcg(&fc_of(w, s.t, l)->maxkey);
+        s.expanded = mk != 0u;
+        s.cutoff = mk ? __fsub_rn(unord_f(mk), s.beam) : INFINITY;
+        if (s.expanded) S.pre_a[l] = (int32_t)((s.d_cur + kTile - 1) / kTile);
+      }
+    }
+    __syncthreads();
+    lane_scan(S.pre_a, L);
+    if (blockIdx.x == 0 && g.has_eps)
+      for (int l = tid; l < L; l += kThreads)
+        if (S.lane[l].phase == kEmit) w.wl_cnt[(size_t)1 * L + l] = 0ull;
+    emit_tiles<1, LP>(a, S);
+
+    // final-arc lattice records (read payload; cleared only after the loop)
+    if (lat) {
+      for (int l = tid; l < L; l += kThreads)
+        S.pre_c[l] = (S.lane[l].phase == kFin) ? S.lane[l].n_cur : 0;
+      __syncthreads();
+      lane_scan(S.pre_c, L);
+      const int total = S.pre_c[L];
+      for (int gi = (int)gstart; gi < total; gi += (int)gstride) {
+        const int l = find_lane(S.pre_c, L, gi);
+        const int32_t p = gi - S.pre_c[l];
+        const SmLane& s = S.lane[l];
+        const int par = s.t & 1;
+        const int32_t d = __ldcg(w.claims + ql(w, par, l) + p);
+        const float fw = __ldg(g.final_w + d);
+        if (fw > -INFINITY) {
+          const float score = key_score(__ldcg(w.payload + pl(w, par, l) + d));
+          LatRec r;
+          r.frame_flags = (s.t << 4) | kRecFinal;
+          r.src_tok = (int32_t)(s.base_cur + p);
+          r.dst_tok = -1;
+          r.src_state = d;
+          r.dst_state = -1;
+          r.arc = (int32_t)(g.A + d);
+          r.end = __fadd_rn(score, fw);
+          r.arcscore = fw;
+          const unsigned long long pos = atomicAdd(&w.lat_cnt[l], 1ull);
+          if (pos < (unsigned long long)w.lat_cap) w.lat[(size_t)l * w.lat_cap + pos] = r;
+          else lane_ovf(a, l, kOvfArena);
+        }
+      }
+    }
+
+    {  // final step (§3) / partial (§8): one CTA per lane walks the winners log
+      if (tid == 0) {
+        int cnt = 0;
+        for (int l = 0; l < L; l++) {
+          S.pre_b[l] = cnt;
+          if (S.lane[l].phase == kFin || S.lane[l].phase == kPart) cnt++;
+        }
+        S.pre_b[L] = cnt;
+      }
+      __syncthreads();
+      const int ntask = S.pre_b[L];
+      for (int task = blockIdx.x; task < ntask; task += G) {
+        const int l = find_lane(S.pre_b, L, task);
+        const SmLane& s = S.lane[l];
+        const int f = s.t, par = f & 1;
+        if (tid == 0) {
+          const FrameCnt* fc = fc_of(w, f, l);
+          const unsigned long long fk = __ldcg(&fc->final_key);
+          const unsigned long long bk = __ldcg(&fc->best_key);
+          int ok = 0, reached = 0, state = -1;
+          float score = -INFINITY;
+          if (s.phase == kFin && fk) {
+            ok = 1; reached = 1; state = key_id(fk); score = key_score(fk);
+          } else if ((s.phase == kPart || a.allow_partial) && bk) {
+            ok = 1;
+            const int32_t arc = key_id(bk);
+            state = arc < 0 ? g.start : __ldg(g.c_dst + arc);
+            score = key_score(bk);
+          }
+          if (__ldcg(&w.lanes[l].overflow) & kOvfArena) ok = 0;
+          int64_t idx = -1;
+          if (ok) idx = s.base_cur + __ldcg(w.tokidx + pl(w, par, l) + state);
+          // walk the winners chain; the newest arc lands at the end of the buffer
+          int64_t n = 0;
+          int32_t* path = w.path + (size_t)l * w.path_cap;
+          const int2* lg = w.wlog + (size_t)l * w.log_cap;
+          int64_t i = idx;
+          const int64_t limit = min(s.cursor, w.log_cap);
+          while (ok && i >= 0 && i < limit && n <= limit) {
+            const int2 e = __ldcg(lg + i);
+            if (e.y < 0) break;
+            if (n < w.path_cap) path[w.path_cap - 1 - n] = e.y;
+            n++;
+            i = e.x;
+          }
+          if (n > w.path_cap) lane_ovf(a, l, kOvfPath);
+          S.bt_n = (int32_t)min(n, w.path_cap);
+          S.bt_ok = ok;
+          S.bt_reached = reached;
+          S.bt_score = ok ? score : -INFINITY;
+          if (lat && s.phase == kFin && ok && !reached) {
+            LatRec r;
+            r.frame_flags = (f << 4) | kRecRedirect;
+            r.src_tok = (int32_t)idx;
+            r.dst_tok = -1;
+            r.src_state = state;
+            r.dst_state = -1;
+            r.arc = (int32_t)(g.A + state);
+            r.end = score;
+            r.arcscore = 0.f;
+            const unsigned long long pos = atomicAdd(&w.lat_cnt[l], 1ull);
+            if (pos < (unsigned long long)w.lat_cap) w.lat[(size_t)l * w.lat_cap + pos] = r;
+            else lane_ovf(a, l, kOvfArena);
+          }
+        }
+        __syncthreads();
+        // words = the path's non-zero output labels, forward order
+        const int n = S.bt_n;
+        const int32_t* path = w.path + (size_t)l * w.path_cap + (w.path_cap - n);
+        int32_t* out = w.words + (size_t)l * a.words_cap;
+        int run = 0;
+        for (int base = 0; base < n; base += kThreads) {
+          const int j = base + tid;
+          int32_t o = 0;
+          if (j < n) o = __ldg(g.c_olabel + __ldcg(path + j));
+          const unsigned bal = __ballot_sync(0xffffffffu, o != 0);
+          if ((tid & 31) == 0) S.scan_tmp[tid >> 5] = __popc(bal);
+          __syncthreads();
+          int wbase = 0, tot = 0;
+          for (int ww = 0; ww < kWarps; ww++) {
+            if (ww < (tid >> 5)) wbase += S.scan_tmp[ww];
+            tot += S.scan_tmp[ww];
+          }
+          const int pos = run + wbase + __popc(bal & lanemask_lt());
+          if (o != 0 && pos < a.words_cap) out[pos] = o;
+          run += tot;
+          __syncthreads();
+        }
+        if (tid == 0) {
+          Result r;
+          r.ok = S.bt_ok;
+          r.reached_final = S.bt_reached;
+          r.overflow = 0;
+          r.n_words = run;
+          r.score = S.bt_score;
+          r.n_arcs = n;
+          r.pad0 = r.pad1 = 0;
+          w.res[l] = r;
+        }
+        __syncthreads();
+      }
+    }
+    if (!grid_sync(a, S, epoch)) return;
+
+    // ================= epsilon closure of the new frames (§5.5)
+    if (g.has_eps) {
+      for (int l = tid; l < L; l += kThreads) {
+        SmLane& s = S.lane[l];
+        s.closure = (s.phase == kEmit && s.expanded) ? s.t + 2 : 0;  // frame t+1
+      }
+      __syncthreads();
+      if (tid == 0) {
+        int anyc = 0;
+        for (int l = 0; l < L; l++) anyc |= S.lane[l].closure;
+        S.flag = anyc;
+      }
+      __syncthreads();
+      if (S.flag && !run_closure(a, S, epoch)) return;
+      for (int l = tid; l < L; l += kThreads) S.lane[l].closure = 0;
+    }
+
+    // ================= lane bookkeeping (identical in every CTA)
+    for (int l = tid; l < L; l += kThreads) {
+      SmLane& s = S.lane[l];
+      s.was_emit = 0;
+      if (s.phase == kEmit) {
+        s.t += 1;
+        s.was_emit = 1;
+      } else if (s.phase == kFin) {
+        s.done_final = 1;
+        s.status = kLaneDone;
+      } else if (s.phase == kPart) {
+        s.done_partial = 1;
+      }
+    }
+    __syncthreads();
+  }
+
+  // ---- lattice backward prune of the lanes finished in this call
+  if (lat) {
+    for (int l = tid; l < L; l += kThreads) {
+      SmLane& s = S.lane[l];
+      const int ovf = __ldcg(&w.lanes[l].overflow);
+      s.closure = (s.done_final && __ldcg(&w.res[l].ok) && !(ovf & (kOvfArena | kOvfKept))) ? 1 : 0;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int any = 0;
+      for (int l = 0; l < L; l++) any |= S.lane[l].closure;
+      S.any = any;
+    }
+    __syncthreads();
+    if (S.any && !lattice_prune(a, S, epoch)) return;
+  }
+
+  // ---- finished lanes: clear the last frame's recombination entries
+  for (int l = 0; l < L; l++) {
+    const SmLane& s = S.lane[l];
+    if (!s.done_final) continue;
+    const int par = s.t & 1;
+    for (int64_t p = gstart; p < s.n_cur; p += gstride) {
+      const int32_t d = __ldcg(w.claims + ql(w, par, l) + p);
+      w.payload[pl(w, par, l) + d] = 0ull;
+    }
+  }
+
+  // ---- write the lane mirrors back
+  if (blockIdx.x == 0) {
+    for (int l = tid; l < L; l += kThreads) {
+      const SmLane& s = S.lane[l];
+      if (s.row < 0) continue;
+      LaneState& st = w.lanes[l];
+      st.t = s.t;
+      st.committed = s.committed;
+      st.beam = s.beam;
+      st.status = s.status;
+      st.cursor = s.cursor;
+      st.base_cur = s.base_cur;
+      st.base_prev = s.base_prev;
+      st.eps_pass = s.eps_pass;
+      st.t_eff = s.t_eff;
+      LaneStats& ls = w.stats[l];
+      ls.frames += s.frames;
+      ls.sum_n += s.sum_n;
+      ls.sum_d += s.sum_d;
+      ls.sum_m += s.sum_m;
+      ls.steps = steps;
+    }
+    if (tid == 0) w.bar->epochs = epoch;
+  }
+}
+
+// ------------------------------------------------------------------ launcher
+
+size_t smem_bytes() { return sizeof(Smem); }
+
+template <typename LP>
+static cudaError_t prepare_t() {
+  return cudaFuncSetAttribute(decode_kernel<LP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sizeof(Smem));
+}
+
+cudaError_t launch_decode(const RunArgs& a, int dtype, int grid, cudaStream_t st) {
+  void* args[] = {(void*)&a};
+  const size_t sm = sizeof(Smem);
+  if (dtype == 1) {
+    cudaError_t e = prepare_t<__half>();
+    if (e != cudaSuccess) return e;
+    return cudaLaunchCooperativeKernel((const void*)decode_kernel<__half>, dim3(grid), dim3(kThreads), args,
+                                       sm, st);
+  }
+  cudaError_t e = prepare_t<float>();
+  if (e != cudaSuccess) return e;
+  return cudaLaunchCooperativeKernel((const void*)decode_kernel<float>, dim3(grid), dim3(kThreads), args, sm,
+                                     st);
+}
+
+cudaError_t max_grid(int dtype, int* grid) {
+  int dev = 0, sms = 0, per = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const size_t sm = sizeof(Smem);
+  if (dtype == 1) {
+    e = prepare_t<__half>();
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, decode_kernel<__half>, kThreads, sm);
+  } else {
+    e = prepare_t<float>();
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, decode_kernel<float>, kThreads, sm);
+  }
+  if (e != cudaSuccess) return e;
+  *grid = per * sms;
+  return cudaSuccess;
+}
+
+}  // namespace wfst
