@@ -180,11 +180,13 @@ def run_gpu(args):
     g = synth.make_graph(args.workload)
     G = W.Graph(g, device=local)
     params = W.make_params(wl.search_beam, wl.output_beam, wl.min_active, wl.max_active, True, False)
-    D = W.Decoder(G, params, wl.B, wl.T)
+    nl = args.lanes or wl.B
+    caps = W.Capacity(0, args.log_cap, 0, 0) if args.log_cap else None
+    D = W.Decoder(G, params, nl, wl.T, caps)
     # each rank decodes its own batch (lanes are independent: weak scaling)
-    lanes = [rank * wl.B + b for b in range(wl.B)]
+    lanes = [rank * nl + b for b in range(nl)]
     lp_host = np.stack([synth.make_lane_log_probs(args.workload, b) for b in lanes])
-    lens = synth.make_lens(args.workload)
+    lens = synth.make_lens(args.workload)[:nl] if nl <= wl.B else np.full(nl, wl.T, np.int32)
     esz = lp_host.itemsize
     lp_dev = torch.from_numpy(lp_host).to(dev)
     lp_pin = torch.from_numpy(lp_host).pin_memory()
@@ -265,6 +267,11 @@ def run_gpu(args):
                      "algorithmic_bytes": int(alg)},
         "e2e": {"value": frames_step * args.steps * ws / e2e_s, "unit": "frames/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "phases_ms": {k[3:]: st0[k] / 1e6 for k in ("ns_init", "ns_max", "ns_expand", "ns_closure",
+                                                     "ns_prune", "ns_prologue", "ns_commit", "ns_clear",
+                                                     "ns_max_tiles", "ns_wait_x", "ns_expand_tiles",
+                                                     "ns_final", "ns_wait_y")},
+        "steps_per_decode": st0["steps"], "barriers_per_decode": st0["barriers"],
         "gpu_launches": args.steps,
         "lanes_ok": res_ok,
         "clocks": clk,
@@ -285,6 +292,8 @@ def main():
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--lanes", type=int, default=0, help="lanes per rank (default: the workload's B)")
+    ap.add_argument("--log-cap", type=int, default=0, help="winners-log entries per lane (0: default)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

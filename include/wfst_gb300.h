@@ -91,7 +91,12 @@ typedef struct {
   int32_t allow_partial;  /* 1: without a final state, return the best frontier token */
   int32_t lattice;        /* 1: persist candidates for wfst_lattice_export */
   int32_t streaming;      /* 1: decoder serves wfst_stream_* (online beam semantics) */
+  int32_t options;        /* WFST_OPT_* bits, 0 = defaults */
 } wfst_params;
+
+/* Turn off the per-token upper-bound skips of the max and expand passes
+ * (§5.3 "Upper-bound skip"; exact either way — for identity tests). */
+#define WFST_OPT_NO_UB_SKIP 1
 
 /* Per-lane capacities; 0 in any field selects its default. */
 typedef struct {
@@ -212,7 +217,16 @@ int wfst_stream_release(wfst_decoder* d, int32_t channel);
 #define WFST_STAT_STEPS 7         /* grid steps of the device loop */
 #define WFST_STAT_BARRIERS 8      /* grid barriers executed */
 #define WFST_STAT_KERNEL_NS 9     /* device time of the decode kernel (ns) */
-#define WFST_STAT_COUNT 10
+#define WFST_STAT_NS_INIT 10      /* device time in lane initialisation + start closure */
+#define WFST_STAT_NS_MAX 11       /* ... in the commit + exact-max phases */
+#define WFST_STAT_NS_EXPAND 12    /* ... in the admission/recombination + final-step phases */
+#define WFST_STAT_NS_CLOSURE 13   /* ... in epsilon-closure passes */
+#define WFST_STAT_NS_PRUNE 14     /* ... in the lattice backward prune */
+/* CTA 0's own timeline inside a frame step (ns): prologue, commit, clear,
+ * max tiles, wait at the first barrier, expand tiles, final-step tasks, wait
+ * at the second barrier */
+#define WFST_STAT_NS_PROLOGUE 15
+#define WFST_STAT_COUNT 23
 int wfst_stats(wfst_decoder* d, int64_t* out, int32_t n);
 
 const char* wfst_last_error(void);

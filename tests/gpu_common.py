@@ -16,10 +16,10 @@ def wl_params(wl, lattice=None, allow_partial=True):
                 allow_partial=allow_partial, lattice=wl.lattice if lattice is None else lattice)
 
 
-def gpu_decoder(W, g, p, max_lanes, max_frames, caps=None, graph=None, streaming=False):
+def gpu_decoder(W, g, p, max_lanes, max_frames, caps=None, graph=None, streaming=False, options=0):
     G = graph if graph is not None else W.Graph(g, device=0)
     params = W.make_params(p["search_beam"], p["output_beam"], p["min_active"], p["max_active"],
-                           p["allow_partial"], p["lattice"], streaming)
+                           p["allow_partial"], p["lattice"], streaming, options)
     return G, W.Decoder(G, params, max_lanes, max_frames, caps)
 
 

@@ -256,3 +256,24 @@ def test_capacity_overflow_is_flagged_and_recovers(W, graphs):
     G2, D2 = gpu_decoder(W, g, p, 2, 50, caps=caps, graph=G)
     out3 = D2.decode(_cuda(lp), lens)
     assert all(o["overflow"] & W.OVF_ARENA for o in out3)
+
+
+def test_upper_bound_skip_is_exact(W, graphs):
+    """The skips of the max and expand passes never change a result: words,
+    scores and the arc statistics are identical with the skips off."""
+    wl = synth.workload(2)
+    g = graphs(2)
+    lanes = list(range(8))
+    lp = synth.make_log_probs(2, lanes=lanes, T=120)
+    lens = np.full(len(lanes), 120, np.int32)
+    p = wl_params(wl)
+    G, D1 = gpu_decoder(W, g, p, len(lanes), 120)
+    _, D0 = gpu_decoder(W, g, p, len(lanes), 120, graph=G, options=W.OPT_NO_UB_SKIP)
+    o1 = D1.decode(_cuda(lp), lens)
+    s1 = D1.stats()
+    o0 = D0.decode(_cuda(lp), lens)
+    s0 = D0.stats()
+    for b in range(len(lanes)):
+        assert list(o1[b]["words"]) == list(o0[b]["words"]) and o1[b]["score"] == o0[b]["score"]
+    for k in ("arcs_expanded", "sum_n", "sum_D", "sum_a", "sum_m"):
+        assert s1[k] == s0[k], k

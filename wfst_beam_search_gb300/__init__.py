@@ -24,7 +24,9 @@ WFST_F32, WFST_F16 = 0, 1
 OVF_ARENA, OVF_KEPT, OVF_PATH = 4, 16, 32
 REC_EPS, REC_FINAL, REC_REDIRECT = 1, 2, 4
 STAT_NAMES = ["frames", "arcs_expanded", "sum_n", "sum_D", "sum_a", "sum_m", "eps",
-              "steps", "barriers", "kernel_ns"]
+              "steps", "barriers", "kernel_ns", "ns_init", "ns_max", "ns_expand", "ns_closure",
+              "ns_prune", "ns_prologue", "ns_commit", "ns_clear", "ns_max_tiles", "ns_wait_x",
+              "ns_expand_tiles", "ns_final", "ns_wait_y"]
 ERRORS = {-1: "INVALID_ARG", -2: "CORRUPT_GRAPH", -3: "CUDA", -4: "OOM", -5: "CAPACITY",
           -6: "TIMEOUT", -7: "STATE"}
 
@@ -53,7 +55,8 @@ class GraphDesc(C.Structure):
 class Params(C.Structure):
     _fields_ = [("search_beam", C.c_float), ("output_beam", C.c_float),
                 ("min_active", C.c_int32), ("max_active", C.c_int32),
-                ("allow_partial", C.c_int32), ("lattice", C.c_int32), ("streaming", C.c_int32)]
+                ("allow_partial", C.c_int32), ("lattice", C.c_int32), ("streaming", C.c_int32),
+                ("options", C.c_int32)]
 
 
 class Capacity(C.Structure):
@@ -230,10 +233,13 @@ class Graph:
             pass
 
 
+OPT_NO_UB_SKIP = 1
+
+
 def make_params(search_beam=20.0, output_beam=8.0, min_active=30, max_active=10000,
-                allow_partial=True, lattice=False, streaming=False) -> Params:
+                allow_partial=True, lattice=False, streaming=False, options=0) -> Params:
     return Params(float(search_beam), float(output_beam), int(min_active), int(max_active),
-                  int(bool(allow_partial)), int(bool(lattice)), int(bool(streaming)))
+                  int(bool(allow_partial)), int(bool(lattice)), int(bool(streaming)), int(options))
 
 
 def _lp_args(lp):

@@ -257,6 +257,7 @@ struct wfst_decoder {
   LaneState* h_lanes = nullptr;
   LaneStats* h_stats = nullptr;
   GridBar* h_bar = nullptr;
+  unsigned long long* h_prof = nullptr;
   int32_t* h_words = nullptr;
   int64_t words_cap_alloc = 0;
   LaneCall* d_calls = nullptr;
@@ -292,6 +293,7 @@ static void decoder_destroy(wfst_decoder* d) {
     if (d->h_lanes) cudaFreeHost(d->h_lanes);
     if (d->h_stats) cudaFreeHost(d->h_stats);
     if (d->h_bar) cudaFreeHost(d->h_bar);
+    if (d->h_prof) cudaFreeHost(d->h_prof);
     if (d->h_words) cudaFreeHost(d->h_words);
     if (d->d_stage) cudaFree(d->d_stage);
     if (d->ev0) cudaEventDestroy(d->ev0);
@@ -350,12 +352,12 @@ extern "C" int wfst_decoder_create(wfst_graph* g, const wfst_params* params, int
   if (e == cudaSuccess) e = dalloc(d, &(ptr), (size_t)(n), z)
   DA(w.payload, 2 * L * N, true);
   DA(w.tokidx, 2 * L * N, false);
-  DA(w.claims, 2 * L * qcap, false);
-  DA(w.arcoff, 2 * L * qcap, false);
+  DA(w.front, 2 * L * qcap, false);
+  DA(w.score, 2 * L * qcap, false);
+  DA(w.maxlp, L * (size_t)std::max(max_frames, 1), false);
   DA(w.tile_first, 2 * L * w.tiles_cap, false);
   if (G.has_eps) {
-    DA(w.wl_state, 2 * L * qcap, false);
-    DA(w.wl_off, 2 * L * qcap, false);
+    DA(w.wl, 2 * L * qcap, false);
     DA(w.wl_tile_first, 2 * L * w.tiles_cap, false);
     DA(w.mark, L * N, true);
   }
@@ -375,6 +377,7 @@ extern "C" int wfst_decoder_create(wfst_graph* g, const wfst_params* params, int
   DA(w.path, L * path_cap, false);
   DA(w.res, L, true);
   DA(w.bar, 1, true);
+  DA(w.prof, kProfSlots, true);
   DA(d->d_calls, L, true);
 #undef DA
   if (e == cudaSuccess) e = cudaMallocHost((void**)&d->h_calls, sizeof(LaneCall) * L);
@@ -382,6 +385,7 @@ extern "C" int wfst_decoder_create(wfst_graph* g, const wfst_params* params, int
   if (e == cudaSuccess) e = cudaMallocHost((void**)&d->h_lanes, sizeof(LaneState) * L);
   if (e == cudaSuccess) e = cudaMallocHost((void**)&d->h_stats, sizeof(LaneStats) * L);
   if (e == cudaSuccess) e = cudaMallocHost((void**)&d->h_bar, sizeof(GridBar));
+  if (e == cudaSuccess) e = cudaMallocHost((void**)&d->h_prof, sizeof(unsigned long long) * kProfSlots);
   if (e == cudaSuccess) e = cudaEventCreate(&d->ev0);
   if (e == cudaSuccess) e = cudaEventCreate(&d->ev1);
   if (e == cudaSuccess) {
@@ -501,7 +505,7 @@ static int run_call(wfst_decoder* d, const void* lp, int32_t dtype, int64_t stri
   a.allow_partial = d->p.allow_partial;
   a.lattice = d->p.lattice;
   a.nblocks = d->grid[dtype == WFST_F16 ? 1 : 0];
-  a.ub_skip = 0;
+  a.ub_skip = (d->p.options & WFST_OPT_NO_UB_SKIP) ? 0 : 1;
   CU(cudaEventRecord(d->ev0, st), "event");
   CU(launch_decode(a, dtype, a.nblocks, st), "decode kernel launch");
   CU(cudaEventRecord(d->ev1, st), "event");
@@ -509,6 +513,8 @@ static int run_call(wfst_decoder* d, const void* lp, int32_t dtype, int64_t stri
   CU(cudaMemcpyAsync(d->h_lanes, w.lanes, sizeof(LaneState) * L, cudaMemcpyDeviceToHost, st), "lanes D2H");
   CU(cudaMemcpyAsync(d->h_stats, w.stats, sizeof(LaneStats) * L, cudaMemcpyDeviceToHost, st), "stats D2H");
   CU(cudaMemcpyAsync(d->h_bar, w.bar, sizeof(GridBar), cudaMemcpyDeviceToHost, st), "barrier D2H");
+  CU(cudaMemcpyAsync(d->h_prof, w.prof, sizeof(unsigned long long) * kProfSlots, cudaMemcpyDeviceToHost, st),
+     "phase timers D2H");
   CU(cudaMemcpyAsync(d->h_words, w.words, sizeof(int32_t) * L * a.words_cap, cudaMemcpyDeviceToHost, st),
      "words D2H");
   CU(cudaStreamSynchronize(st), "decode");
@@ -542,6 +548,12 @@ static int run_call(wfst_decoder* d, const void* lp, int32_t dtype, int64_t stri
   }
   S[WFST_STAT_BARRIERS] = d->h_bar->epochs;
   S[WFST_STAT_KERNEL_NS] = (int64_t)(ms * 1e6);
+  S[WFST_STAT_NS_INIT] = (int64_t)d->h_prof[kProfInit];
+  S[WFST_STAT_NS_MAX] = (int64_t)d->h_prof[kProfCommitMax];
+  S[WFST_STAT_NS_EXPAND] = (int64_t)d->h_prof[kProfExpand];
+  S[WFST_STAT_NS_CLOSURE] = (int64_t)d->h_prof[kProfClosure];
+  S[WFST_STAT_NS_PRUNE] = (int64_t)d->h_prof[kProfPrune];
+  for (int i = 0; i < 8; i++) S[WFST_STAT_NS_PROLOGUE + i] = (int64_t)d->h_prof[kProfPrologue + i];
   return WFST_OK;
 }
 
@@ -728,6 +740,8 @@ extern "C" int wfst_stream_advance(wfst_decoder* d, const int32_t* channels, int
   if (rc != WFST_OK) return rc;
   if (dtype != WFST_F32 && dtype != WFST_F16) return fail(WFST_ERR_INVALID_ARG, "stream_advance: bad dtype");
   if (chunk_T < 0 || (n > 0 && !chunk_lens)) return fail(WFST_ERR_INVALID_ARG, "stream_advance: bad chunk lengths");
+  if (chunk_T > d->max_frames)
+    return fail(WFST_ERR_INVALID_ARG, "stream_advance: chunk_T must not exceed the decoder's max_frames");
   int32_t maxlen = 0;
   for (int32_t i = 0; i < n; i++) {
     if (chunk_lens[i] < 0 || chunk_lens[i] > chunk_T)

@@ -6,8 +6,8 @@
 namespace wfst {
 
 constexpr int kThreads = 512;     // threads per CTA of the persistent kernel
-constexpr int kTile = 2048;       // arc slots per work tile
-constexpr int kTokCap = 2048;     // frontier tokens staged in shared memory per tile chunk
+constexpr int kTile = 128;        // arc slots per work tile (one warp walks one tile)
+constexpr int kTokCap = 128;      // frontier tokens a warp stages in shared memory per chunk
 constexpr int kMaxLanes = 256;    // lanes per decoder
 constexpr int kWarps = kThreads / 32;
 
@@ -112,6 +112,13 @@ struct GridBar {
   unsigned int pad;
 };
 
+struct TokRec {                   // a frontier token (or epsilon worklist entry), 16 bytes
+  int32_t state;
+  uint32_t off;                   // first slot of its arcs in the frame's arc-slot space
+  int32_t row;                    // first internal arc (emitting, or epsilon for worklists)
+  float maxw;                     // max emitting arc weight (upper-bound skip)
+};
+
 struct DevWork {
   int32_t L, N;
   int64_t qcap;                   // frontier capacity per lane per frame
@@ -120,12 +127,12 @@ struct DevWork {
   int32_t lattice, max_frames;
   unsigned long long* payload;    // [2][L][N] recombination keys, 0 = empty
   int32_t* tokidx;                // [2][L][N] position of a state in its frame
-  int32_t* claims;                // [2][L][qcap] states of a frame (the frontier)
-  uint32_t* arcoff;               // [2][L][qcap] emitting-arc offset of each token
+  TokRec* front;                  // [2][L][qcap] tokens of a frame (the frontier), claim order
+  float* score;                   // [2][L][qcap] token scores, staged by the max pass
   int32_t* tile_first;            // [2][L][tiles_cap] token holding each tile's first slot
-  int32_t* wl_state;              // [2][L][qcap] epsilon worklist
-  uint32_t* wl_off;               // [2][L][qcap]
+  TokRec* wl;                     // [2][L][qcap] epsilon worklists
   int32_t* wl_tile_first;         // [2][L][tiles_cap]
+  float* maxlp;                   // [L][max_frames] max log-prob of each row of the call
   uint32_t* mark;                 // [L][N] worklist dedupe marks
   unsigned long long* wl_cnt;     // [3][L] (tokens << 32) | epsilon arcs
   int2* wlog;                     // [L][log_cap] {prev, arc} winners log
@@ -142,7 +149,13 @@ struct DevWork {
   Result* res;                    // [L]
   int32_t* words;                 // [L][words_cap] (words_cap per call)
   GridBar* bar;
+  unsigned long long* prof;       // [kProfSlots] ns per phase kind (CTA 0's view)
 };
+
+// phase timers (ns, summed over a call, measured by CTA 0 thread 0)
+enum ProfSlot { kProfInit = 0, kProfCommitMax, kProfExpand, kProfClosure, kProfPrune, kProfTail,
+                kProfPrologue, kProfCommit, kProfClear, kProfMaxTiles, kProfBarX, kProfExpTiles,
+                kProfFinal, kProfBarY, kProfSlots = 16 };
 
 struct RunArgs {
   DevGraph g;

@@ -12,12 +12,18 @@
 //        all lanes, cut into fixed tiles that every CTA walks (load balance
 //        with one hot lane);
 //   §5.3 pass 1 (max): exact per-lane maximum of end = (score + w) + lp over
-//        every slot; pass 2 (expand): admit end > max - beam and recombine by
-//        destination with one 64-bit atomicMax on (ordered score, lowest arc
-//        id) — a direct-indexed per-lane table replaces the page's hash;
+//        every slot, skipping tokens whose upper bound (score + max weight) +
+//        max log-prob cannot beat an end already posted; pass 2 (expand):
+//        admit end > max - beam and recombine by destination with one 64-bit
+//        atomicMax on (ordered score, lowest arc id) — a direct-indexed
+//        per-lane table replaces the page's hash;
 //   §5.4 commit: each frontier token gets a winners-log entry {prev, arc};
 //   §5.5 epsilon closure by worklist passes to a fixpoint; lattice records;
 //   §7  backtrack from the final token; lattice backward output_beam prune.
+// Work distribution: the arc slots of a frame form tiles of kTile slots; each
+// warp walks its own tiles with no block-level synchronisation, staging the
+// tiles' tokens in its own shared-memory area, and every lane issues the
+// loads of its kSPT slots together (one chain of dependent accesses per tile).
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -26,6 +32,8 @@
 namespace wfst {
 
 constexpr unsigned long long kTimeoutNs = 4000000000ull;  // 4 s per barrier wait
+constexpr int kSPT = kTile / 32;                           // slots per lane per tile
+constexpr int kCB = 4;                                     // tokens per thread per commit batch
 
 enum Phase { kNone = 0, kEmit = 1, kFin = 2, kPart = 3 };
 
@@ -41,7 +49,16 @@ struct SmLane {
   int32_t wl_n, closure;
   int64_t res_lo, res_hi;         // lattice records resolved in this step's commit phase
   unsigned long long frames, sum_n, sum_d, sum_m;
-  int32_t was_emit, pad0;
+  float maxlp, prev_max;          // max log-prob of frame t; the previous step's max end
+  int32_t has_prev, was_emit;
+};
+
+struct WStage {                   // one warp's staged tokens of its current tile
+  uint32_t off[kTokCap + 1];
+  int32_t row[kTokCap];
+  float score[kTokCap];
+  int32_t state[kTokCap];
+  float ub[kTokCap];
 };
 
 struct Smem {
@@ -50,14 +67,12 @@ struct Smem {
   int32_t pre_b[kMaxLanes + 1];   // commit tokens / tasks
   int32_t pre_c[kMaxLanes + 1];   // clear tokens
   int32_t pre_d[kMaxLanes + 1];   // lattice records to resolve
-  uint32_t tok_off[kTokCap + 1];
-  int32_t tok_row[kTokCap];
-  float tok_score[kTokCap];
-  int32_t tok_state[kTokCap];
+  WStage ws[kWarps];
   float redf[kWarps];
   uint32_t redu[kWarps];
   int32_t scan_tmp[kWarps];
   int32_t flag, abort, any, bt_n;
+  unsigned long long prof[kProfSlots + 2];  // CTA 0's phase timers + two time marks
   int64_t bt_idx;
   int32_t bt_ok, bt_reached, bt_state, bt_pad;
   float bt_score;
@@ -97,6 +112,15 @@ __device__ __forceinline__ unsigned lanemask_lt() {
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
   return m;
 }
+__device__ __forceinline__ TokRec ld_tok(const TokRec* p) {
+  const int4 v = __ldcg(reinterpret_cast<const int4*>(p));
+  TokRec r;
+  r.state = v.x;
+  r.off = (uint32_t)v.y;
+  r.row = v.z;
+  r.maxw = __int_as_float(v.w);
+  return r;
+}
 
 template <typename T>
 __device__ __forceinline__ float lp_at(const T* row, int v);
@@ -111,8 +135,18 @@ __device__ __forceinline__ float lp_at<__half>(const __half* row, int v) {
 __device__ __forceinline__ int find_lane(const int32_t* pre, int L, int32_t x) {
   int lo = 0, hi = L;
   while (hi - lo > 1) {
-    int mid = (lo + hi) >> 1;
+    const int mid = (lo + hi) >> 1;
     if (pre[mid] <= x) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Largest i in [0, n) with off[i] <= slot.
+__device__ __forceinline__ int find_tok(const uint32_t* off, int n, uint32_t slot) {
+  int lo = 0, hi = n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (off[mid] <= slot) lo = mid; else hi = mid;
   }
   return lo;
 }
@@ -145,6 +179,16 @@ __device__ void lane_scan(int32_t* pre, int L) {
     if (lane == 31) pre[L] = inc;
   }
   __syncthreads();
+}
+
+// Phase timer: CTA 0 thread 0 charges the time since the last mark (kept in
+// shared memory, slot `from`) to accumulator `slot`.
+__device__ __forceinline__ void prof_mark(unsigned long long* acc, int from, int slot) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    const unsigned long long now = gtimer();
+    acc[slot] += now - acc[kProfSlots + from];
+    acc[kProfSlots + from] = now;
+  }
 }
 
 // Bounded software grid barrier.  Returns false when the launch aborts.
@@ -204,7 +248,7 @@ __device__ __forceinline__ size_t pl(const DevWork& w, int par, int l) {
   return ((size_t)par * w.L + l) * (size_t)w.N;       // payload / tokidx row
 }
 __device__ __forceinline__ size_t ql(const DevWork& w, int par, int l) {
-  return ((size_t)par * w.L + l) * (size_t)w.qcap;    // claims / arcoff / worklists
+  return ((size_t)par * w.L + l) * (size_t)w.qcap;    // front / score / worklists
 }
 __device__ __forceinline__ size_t tl(const DevWork& w, int par, int l) {
   return ((size_t)par * w.L + l) * (size_t)w.tiles_cap;
@@ -213,7 +257,6 @@ __device__ __forceinline__ FrameCnt* fc_of(const DevWork& w, int f, int l) {
   return w.fcnt + (size_t)(f & 3) * w.L + l;
 }
 
-// Warp-wide exclusive scan helper: returns the inclusive prefix of v.
 __device__ __forceinline__ uint32_t warp_inc_scan(uint32_t v) {
   const int lane = threadIdx.x & 31;
   for (int o = 1; o < 32; o <<= 1) {
@@ -223,58 +266,84 @@ __device__ __forceinline__ uint32_t warp_inc_scan(uint32_t v) {
   return v;
 }
 
-// Warp-cooperative append of states to a frontier-like list: one 64-bit
-// atomic per warp returns both the positions and an exclusive prefix of the
-// per-state arc counts (so each token gets a contiguous arc-slot range), and
-// every tile boundary that falls inside a token's range records that token.
-__device__ __forceinline__ void warp_list_append(bool want, int32_t d, uint32_t deg,
-                                                 unsigned long long* ctr, int32_t* states,
-                                                 uint32_t* offs, int32_t* tfirst, int32_t* tokidx,
-                                                 int64_t cap, const RunArgs& a, int l) {
+// Warp-cooperative append of up to K states per thread to a token list (a
+// frame's frontier, EPS = false, or an epsilon worklist, EPS = true).  One
+// 64-bit atomic per warp returns the positions and an exclusive prefix of the
+// states' arc counts (in (k, lane) order), so each token owns a contiguous
+// arc-slot range; each tile boundary inside a token's range records that
+// token.  The per-state row data is re-read in the second pass (an L1 hit)
+// rather than kept live across the atomic.
+template <int K, bool EPS>
+__device__ __forceinline__ void warp_append(const bool (&want)[K], const int32_t (&d)[K],
+                                            unsigned long long* ctr, TokRec* list, int32_t* tfirst,
+                                            int32_t* tokidx, int64_t cap, const RunArgs& a, int l) {
   const unsigned full = 0xffffffffu;
-  const unsigned m = __ballot_sync(full, want);
-  if (!m) return;
-  const int lane = threadIdx.x & 31;
-  const uint32_t dv = want ? deg : 0u;
-  const uint32_t inc = warp_inc_scan(dv);
-  const uint32_t total = __shfl_sync(full, inc, 31);
-  const int leader = __ffs(m) - 1;
-  unsigned long long base = 0;
-  if (lane == leader) base = atomicAdd(ctr, ((unsigned long long)__popc(m) << 32) | total);
-  base = __shfl_sync(full, base, leader);
-  if (want) {
-    const uint32_t p = (uint32_t)(base >> 32) + __popc(m & lanemask_lt());
-    const uint32_t off = (uint32_t)base + inc - dv;
-    if (p < (uint64_t)cap) {
-      states[p] = d;
-      offs[p] = off;
-      if (tokidx) tokidx[d] = (int32_t)p;
-      if (dv > 0) {
-        const uint32_t k0 = (off + kTile - 1) / kTile, k1 = (off + dv - 1) / kTile;
-        for (uint32_t k = k0; k <= k1; k++) tfirst[k] = (int32_t)p;
-      }
-    } else {
-      lane_ovf(a, l, kOvfKept);
+  uint32_t cnt_sum = 0, tot_sum = 0;
+#pragma unroll
+  for (int k = 0; k < K; k++) {
+    cnt_sum += __popc(__ballot_sync(full, want[k]));
+    uint32_t v = 0;
+    if (want[k]) {
+      const int4 m = __ldg(a.g.meta + d[k]);
+      v = EPS ? (uint32_t)(m.z - m.y) : (uint32_t)(m.y - m.x);
     }
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(full, v, o);
+    tot_sum += v;
+  }
+  if (!cnt_sum) return;
+  const int lane = threadIdx.x & 31;
+  unsigned long long base = 0;
+  if (lane == 0) base = atomicAdd(ctr, ((unsigned long long)cnt_sum << 32) | tot_sum);
+  base = __shfl_sync(full, base, 0);
+  uint32_t pb = (uint32_t)(base >> 32), ob = (uint32_t)base;
+  const unsigned lt = lanemask_lt();
+#pragma unroll
+  for (int k = 0; k < K; k++) {
+    const unsigned m = __ballot_sync(full, want[k]);
+    int4 md = make_int4(0, 0, 0, 0);
+    if (want[k]) md = __ldg(a.g.meta + d[k]);
+    const uint32_t dv = EPS ? (uint32_t)(md.z - md.y) : (uint32_t)(md.y - md.x);
+    const uint32_t inc = warp_inc_scan(dv);
+    if (want[k]) {
+      const uint32_t p = pb + __popc(m & lt);
+      const uint32_t off = ob + inc - dv;
+      if (p < (uint64_t)cap) {
+        *reinterpret_cast<int4*>(list + p) = make_int4(d[k], (int)off, EPS ? md.y : md.x, EPS ? 0 : md.w);
+        if (tokidx) tokidx[d[k]] = (int32_t)p;
+        if (dv > 0) {
+          const uint32_t k0 = (off + kTile - 1) / kTile, k1 = (off + dv - 1) / kTile;
+          for (uint32_t q = k0; q <= k1; q++) tfirst[q] = (int32_t)p;
+        }
+      } else {
+        lane_ovf(a, l, kOvfKept);
+      }
+    }
+    pb += __popc(m);
+    ob += __shfl_sync(full, inc, 31);
   }
 }
 
-// Claim states into frame f of lane l (and seed the epsilon worklist W0).
-__device__ __forceinline__ void warp_claim(const RunArgs& a, bool want, int32_t d, int l, int f,
-                                           bool seed_worklist) {
+// Claim states into frame f of lane l (and seed the epsilon worklist W0 with
+// the claimed states that have epsilon arcs).
+template <int K>
+__device__ __forceinline__ void warp_claim(const RunArgs& a, const bool (&want)[K], const int32_t (&d)[K],
+                                           int l, int f, bool seed_worklist) {
   const DevWork& w = a.w;
-  const unsigned m = __ballot_sync(0xffffffffu, want);
-  if (!m) return;
-  int4 meta = make_int4(0, 0, 0, 0);
-  if (want) meta = __ldg(a.g.meta + d);
   const int par = f & 1;
-  warp_list_append(want, d, (uint32_t)(meta.y - meta.x), &fc_of(w, f, l)->cnt,
-                   w.claims + ql(w, par, l), w.arcoff + ql(w, par, l), w.tile_first + tl(w, par, l),
-                   w.tokidx + pl(w, par, l), w.qcap, a, l);
+  warp_append<K, false>(want, d, &fc_of(w, f, l)->cnt, w.front + ql(w, par, l), w.tile_first + tl(w, par, l),
+                        w.tokidx + pl(w, par, l), w.qcap, a, l);
   if (a.g.has_eps && seed_worklist) {
-    const bool ws = want && (meta.z > meta.y);
-    warp_list_append(ws, d, (uint32_t)(meta.z - meta.y), &w.wl_cnt[l], w.wl_state + ql(w, 0, l),
-                     w.wl_off + ql(w, 0, l), w.wl_tile_first + tl(w, 0, l), nullptr, w.qcap, a, l);
+    bool ws[K];
+#pragma unroll
+    for (int k = 0; k < K; k++) {
+      ws[k] = false;
+      if (want[k]) {
+        const int4 m = __ldg(a.g.meta + d[k]);
+        ws[k] = m.z > m.y;
+      }
+    }
+    warp_append<K, true>(ws, d, &w.wl_cnt[l], w.wl + ql(w, 0, l), w.wl_tile_first + tl(w, 0, l), nullptr,
+                         w.qcap, a, l);
   }
 }
 
@@ -298,17 +367,21 @@ __device__ __forceinline__ void warp_lat_append(const RunArgs& a, bool want, int
 
 // ------------------------------------------------------------------ emitting tiles
 
-// MODE 0: exact per-lane max of end over the frame's emitting arcs.
-// MODE 1: admission against the cutoff + recombination into the next frame.
+// MODE 0 (max): exact per-lane max of end over the frame's emitting arcs;
+//   stages every token's score for MODE 1.
+// MODE 1 (expand): admission against the cutoff + recombination into the
+//   next frame.
 template <int MODE, typename LP>
 __device__ void emit_tiles(const RunArgs& a, Smem& S) {
   const DevWork& w = a.w;
   const DevGraph& g = a.g;
   const int L = a.nlanes;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  WStage& ws = S.ws[warp];
   const int total = S.pre_a[L];
   const LP* lpb = reinterpret_cast<const LP*>(a.lp);
-  for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+  const int nw = gridDim.x * kWarps;
+  for (int tile = blockIdx.x * kWarps + warp; tile < total; tile += nw) {
     const int l = find_lane(S.pre_a, L, tile);
     const int k = tile - S.pre_a[l];
     const SmLane& s = S.lane[l];
@@ -320,81 +393,111 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
     int32_t p_hi = (k + 1 < ntiles) ? __ldcg(w.tile_first + tl(w, par, l) + k + 1) + 1 : s.n_cur;
     if (p_hi > s.n_cur) p_hi = s.n_cur;
     const LP* row = lpb + (int64_t)s.row * a.stride_b + (int64_t)(f - s.t0) * a.stride_t;
-    const float cutoff = s.cutoff;
     const size_t q = ql(w, par, l);
     const size_t pay = pl(w, par, l);
-    const size_t npay = pl(w, par ^ 1, l);
+    const float maxlp = s.maxlp;
+    // the skip threshold: an end already achieved (max) / the cutoff (expand)
+    float thr = s.cutoff;
+    if (MODE == 0) {
+      unsigned ek = lane == 0 ? __ldcg(&fc_of(w, f, l)->maxkey) : 0u;
+      ek = __shfl_sync(0xffffffffu, ek, 0);
+      thr = ek ? unord_f(ek) : -INFINITY;
+    }
     float vmax = -INFINITY;
     uint32_t admitted = 0;
     for (int32_t c = p_lo; c < p_hi; c += kTokCap) {
       const int ntok = min(kTokCap, p_hi - c);
-      __syncthreads();
-      for (int i = tid; i < ntok; i += kThreads) {
-        const int32_t p = c + i;
-        const int32_t d = __ldcg(w.claims + q + p);
-        S.tok_off[i] = __ldcg(w.arcoff + q + p);
-        S.tok_row[i] = __ldg(&g.meta[d].x);
-        S.tok_score[i] = key_score(__ldcg(w.payload + pay + d));
-        S.tok_state[i] = d;
-      }
-      if (tid == 0) S.tok_off[ntok] = (c + ntok < s.n_cur) ? __ldcg(w.arcoff + q + c + ntok) : s.d_cur;
-      __syncthreads();
-      const uint32_t c_lo = max(s_lo, S.tok_off[0]);
-      const uint32_t c_hi = min(s_hi, S.tok_off[ntok]);
-      for (uint32_t base = c_lo + warp * 32; base < c_hi; base += kThreads) {
-        const uint32_t slot = base + lane;
-        const bool valid = slot < c_hi;
-        float end = -INFINITY, arcsc = 0.f;
-        int32_t ai = 0, i = 0;
-        if (valid) {
-          int lo = 0, hi = ntok;  // largest i with tok_off[i] <= slot
-          while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (S.tok_off[mid] <= slot) lo = mid; else hi = mid;
+      __syncwarp();
+#pragma unroll
+      for (int r = 0; r < kTokCap / 32; r++) {
+        const int i = r * 32 + lane;
+        if (i < ntok) {
+          const TokRec tr = ld_tok(w.front + q + c + i);
+          float sc;
+          if (MODE == 0) {
+            sc = key_score(__ldcg(w.payload + pay + tr.state));
+            w.score[q + c + i] = sc;
+          } else {
+            sc = __ldcg(w.score + q + c + i);
           }
-          i = lo;
-          ai = S.tok_row[i] + (int32_t)(slot - S.tok_off[i]);
-          const int il = __ldg(g.ilabel + ai);
-          const float wt = __ldg(g.weight + ai);
-          const float lpv = lp_at<LP>(row, il);
-          end = __fadd_rn(__fadd_rn(S.tok_score[i], wt), lpv);
-          arcsc = __fadd_rn(wt, lpv);
+          ws.off[i] = tr.off;
+          ws.row[i] = tr.row;
+          ws.score[i] = sc;
+          ws.state[i] = tr.state;
+          ws.ub[i] = __fadd_rn(__fadd_rn(sc, tr.maxw), maxlp);
         }
-        if (MODE == 0) {
-          vmax = fmaxf(vmax, end);
-        } else {
-          const bool adm = valid && (end > cutoff);
-          bool claim = false;
-          int32_t d = 0, id = 0;
-          if (adm) {
-            admitted++;
-            d = __ldg(g.dst + ai);
-            id = g.identity ? ai : __ldg(g.arc_id + ai);
-            const unsigned long long old = atomicMax(w.payload + npay + d, mk_key(end, id));
-            claim = (old == 0ull);
-          }
-          warp_claim(a, claim, d, l, f + 1, true);
-          if (a.lattice) {
+      }
+      if (lane == 0) ws.off[ntok] = (c + ntok < s.n_cur) ? ld_tok(w.front + q + c + ntok).off : s.d_cur;
+      __syncwarp();
+      const uint32_t c_lo = max(s_lo, ws.off[0]);
+      const uint32_t c_hi = min(s_hi, ws.off[ntok]);
+      int ti[kSPT];
+      bool act[kSPT];
+      int32_t ai[kSPT];
+#pragma unroll
+      for (int j = 0; j < kSPT; j++) {
+        const uint32_t slot = c_lo + (uint32_t)(j * 32 + lane);
+        act[j] = slot < c_hi;
+        ti[j] = act[j] ? find_tok(ws.off, ntok, slot) : 0;
+        if (act[j] && a.ub_skip && ws.ub[ti[j]] <= thr) act[j] = false;
+        ai[j] = act[j] ? ws.row[ti[j]] + (int32_t)(slot - ws.off[ti[j]]) : 0;
+      }
+      int il[kSPT];
+      float wt[kSPT];
+#pragma unroll
+      for (int j = 0; j < kSPT; j++) {
+        il[j] = act[j] ? (int)__ldg(g.ilabel + ai[j]) : 0;
+        wt[j] = act[j] ? __ldg(g.weight + ai[j]) : 0.f;
+      }
+      float end[kSPT];
+#pragma unroll
+      for (int j = 0; j < kSPT; j++) {
+        const float lpv = act[j] ? lp_at<LP>(row, il[j]) : 0.f;
+        end[j] = act[j] ? __fadd_rn(__fadd_rn(ws.score[ti[j]], wt[j]), lpv) : -INFINITY;
+        if (MODE == 1 && a.lattice) wt[j] = __fadd_rn(wt[j], lpv);  // the record's own score
+      }
+      if (MODE == 0) {
+#pragma unroll
+        for (int j = 0; j < kSPT; j++) vmax = fmaxf(vmax, end[j]);
+      } else {
+        const size_t npay = pl(w, par ^ 1, l);
+        bool adm[kSPT], claim[kSPT];
+        int32_t d[kSPT], id[kSPT];
+#pragma unroll
+        for (int j = 0; j < kSPT; j++) {
+          adm[j] = act[j] && (end[j] > thr);
+          d[j] = adm[j] ? __ldg(g.dst + ai[j]) : 0;
+          id[j] = adm[j] ? (g.identity ? ai[j] : __ldg(g.arc_id + ai[j])) : 0;
+        }
+        if (a.lattice) {
+#pragma unroll
+          for (int j = 0; j < kSPT; j++) {
             LatRec r;
             r.frame_flags = f << 4;
-            r.src_tok = (int32_t)(s.base_cur + (c + i));
+            r.src_tok = (int32_t)(s.base_cur + (c + ti[j]));
             r.dst_tok = -1;
-            r.src_state = S.tok_state[i];
-            r.dst_state = d;
-            r.arc = id;
-            r.end = end;
-            r.arcscore = arcsc;
-            warp_lat_append(a, adm, l, r);
+            r.src_state = ws.state[ti[j]];
+            r.dst_state = d[j];
+            r.arc = id[j];
+            r.end = end[j];
+            r.arcscore = wt[j];
+            warp_lat_append(a, adm[j], l, r);
           }
         }
+#pragma unroll
+        for (int j = 0; j < kSPT; j++) {
+          claim[j] = adm[j] && atomicMax(w.payload + npay + d[j], mk_key(end[j], id[j])) == 0ull;
+          admitted += adm[j] ? 1u : 0u;
+        }
+        warp_claim<kSPT>(a, claim, d, l, f + 1, true);
       }
     }
     if (MODE == 0) {
-      const float bm = block_max_f(vmax, S);
-      if (tid == 0) atomicMax(&fc_of(w, f, l)->maxkey, ord_f(bm));
+      for (int o = 16; o; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+      if (lane == 0 && vmax > -INFINITY) atomicMax(&fc_of(w, f, l)->maxkey, ord_f(vmax));
     } else {
-      const uint32_t ad = block_sum_u(admitted, S);
-      if (tid == 0 && ad) atomicAdd(&w.stats[l].sum_a, (unsigned long long)ad);
+      for (int o = 16; o; o >>= 1) admitted += __shfl_xor_sync(0xffffffffu, admitted, o);
+      if (lane == 0 && admitted) atomicAdd(&w.stats[l].sum_a, (unsigned long long)admitted);
     }
   }
 }
@@ -408,14 +511,15 @@ __device__ void eps_tiles(const RunArgs& a, Smem& S, int buf, int next_slot) {
   const DevWork& w = a.w;
   const DevGraph& g = a.g;
   const int L = a.nlanes;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  WStage& ws = S.ws[warp];
   const int total = S.pre_a[L];
-  for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+  const int nw = gridDim.x * kWarps;
+  for (int tile = blockIdx.x * kWarps + warp; tile < total; tile += nw) {
     const int l = find_lane(S.pre_a, L, tile);
     const int k = tile - S.pre_a[l];
     const SmLane& s = S.lane[l];
-    const int f = s.closure;        // closure frame + 1
-    const int fr = f - 1;
+    const int fr = s.closure - 1;  // closure frame
     const int par = fr & 1;
     const int ntiles = S.pre_a[l + 1] - S.pre_a[l];
     const uint32_t s_lo = (uint32_t)k * kTile;
@@ -429,70 +533,79 @@ __device__ void eps_tiles(const RunArgs& a, Smem& S, int buf, int next_slot) {
     const uint32_t pass_id = s.eps_pass + 1;
     for (int32_t c = p_lo; c < p_hi; c += kTokCap) {
       const int ntok = min(kTokCap, p_hi - c);
-      __syncthreads();
-      for (int i = tid; i < ntok; i += kThreads) {
-        const int32_t p = c + i;
-        const int32_t u = __ldcg(w.wl_state + q + p);
-        S.tok_off[i] = __ldcg(w.wl_off + q + p);
-        S.tok_row[i] = __ldg(&g.meta[u].y);  // first epsilon arc
-        S.tok_score[i] = key_score(__ldcg(w.payload + pay + u));
-        S.tok_state[i] = u;
-      }
-      if (tid == 0) S.tok_off[ntok] = (c + ntok < s.wl_n) ? __ldcg(w.wl_off + q + c + ntok) : s.wl_e;
-      __syncthreads();
-      const uint32_t c_lo = max(s_lo, S.tok_off[0]);
-      const uint32_t c_hi = min(s_hi, S.tok_off[ntok]);
-      for (uint32_t base = c_lo + warp * 32; base < c_hi; base += kThreads) {
-        const uint32_t slot = base + lane;
-        const bool valid = slot < c_hi;
-        bool adm = false, claim = false, wl = false;
-        int32_t d = 0, id = 0, i = 0;
-        float e = 0.f, wt = 0.f;
-        uint32_t edeg = 0;
-        if (valid) {
-          int lo = 0, hi = ntok;
-          while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (S.tok_off[mid] <= slot) lo = mid; else hi = mid;
-          }
-          i = lo;
-          const int32_t ai = S.tok_row[i] + (int32_t)(slot - S.tok_off[i]);
-          wt = __ldg(g.weight + ai);
-          e = __fadd_rn(S.tok_score[i], wt);
-          if (e > cutoff) {
-            adm = true;
-            d = __ldg(g.dst + ai);
-            id = g.identity ? ai : __ldg(g.arc_id + ai);
-            const unsigned long long key = mk_key(e, id);
-            const unsigned long long old = atomicMax(w.payload + pay + d, key);
-            claim = (old == 0ull);
-            if (key > old) {
-              const int4 md = __ldg(g.meta + d);
-              if (md.z > md.y) {
-                const uint32_t prevmark = atomicExch(w.mark + (size_t)l * w.N + d, pass_id);
-                wl = (prevmark != pass_id);
-                edeg = (uint32_t)(md.z - md.y);
-              }
-            }
-          }
+      __syncwarp();
+#pragma unroll
+      for (int r = 0; r < kTokCap / 32; r++) {
+        const int i = r * 32 + lane;
+        if (i < ntok) {
+          const TokRec tr = ld_tok(w.wl + q + c + i);
+          ws.off[i] = tr.off;
+          ws.row[i] = tr.row;  // first epsilon arc
+          ws.score[i] = key_score(__ldcg(w.payload + pay + tr.state));
+          ws.state[i] = tr.state;
         }
-        warp_claim(a, claim, d, l, fr, false);
-        warp_list_append(wl, d, edeg, &w.wl_cnt[(size_t)next_slot * L + l], w.wl_state + ql(w, buf ^ 1, l),
-                         w.wl_off + ql(w, buf ^ 1, l), w.wl_tile_first + tl(w, buf ^ 1, l), nullptr,
-                         w.qcap, a, l);
-        if (a.lattice) {
+      }
+      if (lane == 0) ws.off[ntok] = (c + ntok < s.wl_n) ? ld_tok(w.wl + q + c + ntok).off : s.wl_e;
+      __syncwarp();
+      const uint32_t c_lo = max(s_lo, ws.off[0]);
+      const uint32_t c_hi = min(s_hi, ws.off[ntok]);
+      int ti[kSPT];
+      bool act[kSPT];
+      int32_t ai[kSPT];
+#pragma unroll
+      for (int j = 0; j < kSPT; j++) {
+        const uint32_t slot = c_lo + (uint32_t)(j * 32 + lane);
+        act[j] = slot < c_hi;
+        ti[j] = act[j] ? find_tok(ws.off, ntok, slot) : 0;
+        ai[j] = act[j] ? ws.row[ti[j]] + (int32_t)(slot - ws.off[ti[j]]) : 0;
+      }
+      float wt[kSPT], e[kSPT];
+      bool adm[kSPT];
+      int32_t d[kSPT], id[kSPT];
+#pragma unroll
+      for (int j = 0; j < kSPT; j++) wt[j] = act[j] ? __ldg(g.weight + ai[j]) : 0.f;
+#pragma unroll
+      for (int j = 0; j < kSPT; j++) {
+        e[j] = __fadd_rn(ws.score[ti[j]], wt[j]);
+        adm[j] = act[j] && (e[j] > cutoff);
+        d[j] = adm[j] ? __ldg(g.dst + ai[j]) : 0;
+        id[j] = adm[j] ? (g.identity ? ai[j] : __ldg(g.arc_id + ai[j])) : 0;
+      }
+      if (a.lattice) {
+#pragma unroll
+        for (int j = 0; j < kSPT; j++) {
           LatRec r;
           r.frame_flags = (fr << 4) | kRecEps;
-          r.src_tok = __float_as_int(S.tok_score[i]);  // score used; checked at resolution
+          r.src_tok = __float_as_int(ws.score[ti[j]]);  // score used; checked at resolution
           r.dst_tok = -1;
-          r.src_state = S.tok_state[i];
-          r.dst_state = d;
-          r.arc = id;
-          r.end = e;
-          r.arcscore = wt;
-          warp_lat_append(a, adm, l, r);
+          r.src_state = ws.state[ti[j]];
+          r.dst_state = d[j];
+          r.arc = id[j];
+          r.end = e[j];
+          r.arcscore = wt[j];
+          warp_lat_append(a, adm[j], l, r);
         }
       }
+      bool claim[kSPT], better[kSPT];
+#pragma unroll
+      for (int j = 0; j < kSPT; j++) {
+        const unsigned long long key = mk_key(e[j], id[j]);
+        const unsigned long long old = adm[j] ? atomicMax(w.payload + pay + d[j], key) : ~0ull;
+        claim[j] = adm[j] && old == 0ull;
+        better[j] = adm[j] && key > old;
+      }
+      warp_claim<kSPT>(a, claim, d, l, fr, false);
+      bool wl[kSPT];
+#pragma unroll
+      for (int j = 0; j < kSPT; j++) {
+        wl[j] = false;
+        if (better[j]) {
+          const int4 m = __ldg(g.meta + d[j]);
+          if (m.z > m.y) wl[j] = atomicExch(w.mark + (size_t)l * w.N + d[j], pass_id) != pass_id;
+        }
+      }
+      warp_append<kSPT, true>(wl, d, &w.wl_cnt[(size_t)next_slot * L + l], w.wl + ql(w, buf ^ 1, l),
+                              w.wl_tile_first + tl(w, buf ^ 1, l), nullptr, w.qcap, a, l);
     }
   }
 }
@@ -560,18 +673,37 @@ __device__ void init_lane_global(const RunArgs& a, int l) {
   const int4 m = __ldg(g.meta + s0);
   const uint32_t deg = (uint32_t)(m.y - m.x);
   w.payload[pl(w, 0, l) + s0] = mk_key(0.0f, -1);
-  w.claims[ql(w, 0, l)] = s0;
-  w.arcoff[ql(w, 0, l)] = 0u;
+  *reinterpret_cast<int4*>(w.front + ql(w, 0, l)) = make_int4(s0, 0, m.x, m.w);
   w.tokidx[pl(w, 0, l) + s0] = 0;
   if (deg > 0)
     for (uint32_t k = 0; k <= (deg - 1) / kTile; k++) w.tile_first[tl(w, 0, l) + k] = 0;
   w.fcnt[l].cnt = (1ull << 32) | deg;
   if (g.has_eps && m.z > m.y) {
     const uint32_t edeg = (uint32_t)(m.z - m.y);
-    w.wl_state[ql(w, 0, l)] = s0;
-    w.wl_off[ql(w, 0, l)] = 0u;
+    *reinterpret_cast<int4*>(w.wl + ql(w, 0, l)) = make_int4(s0, 0, m.y, 0);
     for (uint32_t k = 0; k <= (edeg - 1) / kTile; k++) w.wl_tile_first[tl(w, 0, l) + k] = 0;
     w.wl_cnt[l] = (1ull << 32) | edeg;
+  }
+}
+
+// Row maxima of the call's log-probs (one warp per row): the acoustic half
+// of the per-token upper bound.
+template <typename LP>
+__device__ void row_maxima(const RunArgs& a, Smem& S) {
+  const DevWork& w = a.w;
+  const int L = a.nlanes;
+  const int total = S.pre_a[L];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const LP* lpb = reinterpret_cast<const LP*>(a.lp);
+  const int V = a.g.V;
+  for (int r = blockIdx.x * kWarps + warp; r < total; r += gridDim.x * kWarps) {
+    const int l = find_lane(S.pre_a, L, r);
+    const int j = r - S.pre_a[l];
+    const LP* row = lpb + (int64_t)S.lane[l].row * a.stride_b + (int64_t)j * a.stride_t;
+    float m = -INFINITY;
+    for (int v = lane; v < V; v += 32) m = fmaxf(m, lp_at<LP>(row, v));
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) w.maxlp[(size_t)l * w.max_frames + j] = m;
   }
 }
 
@@ -693,8 +825,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
   const int64_t gstride = (int64_t)G * kThreads;
   const int64_t gstart = (int64_t)blockIdx.x * kThreads + tid;
   const bool lat = a.lattice != 0;
+  const LP* lpb = reinterpret_cast<const LP*>(a.lp);
   unsigned epoch = 0;
   unsigned long long steps = 0;
+  unsigned long long* prof = S.prof;
+  if (tid < kProfSlots) prof[tid] = 0;
+  if (tid == 0) prof[kProfSlots] = prof[kProfSlots + 1] = gtimer();
+  const int tlast = 0, tsub = 1;
 
   // ---- lane mirrors (every CTA holds an identical copy)
   for (int l = tid; l < L; l += kThreads) {
@@ -713,6 +850,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     s.row = c.row;
     s.flags = c.row >= 0 ? c.flags : 0;
     s.phase = kNone;
+    s.need_commit = 0;
     s.done_final = s.done_partial = 0;
     s.frames = s.sum_n = s.sum_d = s.sum_m = 0;
     s.was_emit = 0;
@@ -730,22 +868,27 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     }
     s.t0 = s.t;
     s.t_end = s.t + (c.row >= 0 ? c.nframes : 0);
+    S.pre_a[l] = (c.row >= 0 && s.status == kLaneRunning) ? c.nframes : 0;
   }
   __syncthreads();
 
-  // ---- lane initialisation + start-frontier closure (cutoff 0 - search_beam)
+  // ---- lane initialisation and the call's row maxima, then the start
+  //      frontier's closure (cutoff 0 - search_beam)
+  lane_scan(S.pre_a, L);
   if (tid == 0) {
     int any = 0;
     for (int l = 0; l < L; l++) any |= (S.lane[l].flags & kCallInit);
     S.any = any;
+    S.flag = S.pre_a[L] > 0;
   }
   __syncthreads();
-  if (S.any) {
+  if (S.any || S.flag) {
     if (tid == 0)
       for (int l = blockIdx.x; l < L; l += G)
         if (S.lane[l].flags & kCallInit) init_lane_global(a, l);
+    row_maxima<LP>(a, S);
     if (!grid_sync(a, S, epoch)) return;
-    if (g.has_eps) {
+    if (S.any && g.has_eps) {
       for (int l = tid; l < L; l += kThreads) {
         SmLane& s = S.lane[l];
         s.closure = (s.flags & kCallInit) ? 1 : 0;  // frame 0
@@ -757,6 +900,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
       __syncthreads();
     }
   }
+  prof_mark(prof, tlast, kProfInit);
 
   // ---- the frame loop
   for (;;) {
@@ -781,10 +925,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
       s.d_cur = (uint32_t)cnt;
       if (n_raw > (unsigned long long)w.qcap) {
         // tokens past the capacity were dropped: their slots are the tail
-        const size_t q = ql(w, s.t & 1, l);
-        const int32_t lastd = __ldcg(w.claims + q + s.n_cur - 1);
-        const int4 m = __ldg(g.meta + lastd);
-        s.d_cur = __ldcg(w.arcoff + q + s.n_cur - 1) + (uint32_t)(m.y - m.x);
+        const TokRec r = ld_tok(w.front + ql(w, s.t & 1, l) + s.n_cur - 1);
+        const int4 m = __ldg(g.meta + r.state);
+        s.d_cur = r.off + (uint32_t)(m.y - m.x);
       }
       s.n_prev = 0;
       if (s.t >= 1 && s.phase != kPart) {
@@ -810,6 +953,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         s.frames += 1;
         s.sum_n += n_raw;
         s.sum_d += s.d_cur;
+        s.maxlp = __ldcg(w.maxlp + (size_t)l * w.max_frames + (s.t - s.t0));
+        const unsigned pk = s.t >= 1 ? __ldcg(&fc_of(w, s.t - 1, l)->maxkey) : 0u;
+        s.has_prev = pk != 0u;
+        s.prev_max = pk ? unord_f(pk) : -INFINITY;
       }
       S.pre_b[l] = (s.need_commit || s.phase == kFin || s.phase == kPart) ? s.n_cur : 0;
       S.pre_c[l] = s.n_prev;
@@ -835,6 +982,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     lane_scan(S.pre_b, L);
     lane_scan(S.pre_c, L);
     lane_scan(S.pre_d, L);
+    prof_mark(prof, tsub, kProfPrologue);
 
     // ================= phase X: commit frame t, clear frame t-1, exact max
     if (blockIdx.x == 0) {
@@ -850,53 +998,100 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
           w.lat_groups[(size_t)l * (w.max_frames + 2) + s.t] = s.res_hi;
       }
     }
-    {  // commit (§5.4): winners-log entry {prev, arc} per token; final-step keys
+    {  // commit (§5.4): winners-log entry {prev, arc} per token; final-step
+       // keys; a best token of an emitting lane seeds the exact max
       const int total = S.pre_b[L];
-      for (int gi = (int)gstart; gi < total; gi += (int)gstride) {
-        const int l = find_lane(S.pre_b, L, gi);
-        const int32_t p = gi - S.pre_b[l];
-        const SmLane& s = S.lane[l];
-        const int f = s.t, par = f & 1;
-        const int32_t d = __ldcg(w.claims + ql(w, par, l) + p);
-        const unsigned long long key = __ldcg(w.payload + pl(w, par, l) + d);
-        const int32_t arc = key_id(key);
-        const float score = key_score(key);
-        if (s.need_commit) {
-          const int64_t base_new = s.cursor;   // frame f
-          const int64_t base_old = s.base_cur; // frame f-1
-          int32_t prev = -1;
-          if (arc >= 0) {
-            const int32_t se = __ldg(g.c_src + arc);
-            const int32_t src = se & 0x7fffffff;
-            if (se < 0) prev = (int32_t)(base_new + __ldcg(w.tokidx + pl(w, par, l) + src));
-            else prev = (int32_t)(base_old + __ldcg(w.tokidx + pl(w, par ^ 1, l) + src));
-          }
-          const int64_t idx = base_new + p;
-          if (idx < w.log_cap) w.wlog[(size_t)l * w.log_cap + idx] = make_int2(prev, arc);
-          else lane_ovf(a, l, kOvfArena);
-          if (g.has_eps) {
-            const int4 m = __ldg(g.meta + d);
-            if (m.z > m.y) atomicAdd(&w.stats[l].eps, (unsigned long long)(m.z - m.y));
+      for (int g0 = blockIdx.x * kThreads * kCB + tid; g0 < total; g0 += G * kThreads * kCB) {
+        int lk[kCB];
+        int32_t pk[kCB], st[kCB];
+        bool v[kCB];
+        unsigned long long key[kCB];
+#pragma unroll
+        for (int k = 0; k < kCB; k++) {
+          const int gi = g0 + k * kThreads;
+          v[k] = gi < total;
+          lk[k] = v[k] ? find_lane(S.pre_b, L, gi) : 0;
+          pk[k] = v[k] ? gi - S.pre_b[lk[k]] : 0;
+          st[k] = v[k] ? __ldcg(&w.front[ql(w, S.lane[lk[k]].t & 1, lk[k]) + pk[k]].state) : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < kCB; k++)
+          key[k] = v[k] ? __ldcg(w.payload + pl(w, S.lane[lk[k]].t & 1, lk[k]) + st[k]) : 0ull;
+        int32_t se[kCB];
+#pragma unroll
+        for (int k = 0; k < kCB; k++) {
+          const int32_t arc = key_id(key[k]);
+          se[k] = (v[k] && S.lane[lk[k]].need_commit && arc >= 0) ? __ldg(g.c_src + arc) : 0;
+        }
+        int32_t tix[kCB];
+#pragma unroll
+        for (int k = 0; k < kCB; k++) {
+          const int32_t arc = key_id(key[k]);
+          tix[k] = 0;
+          if (v[k] && S.lane[lk[k]].need_commit && arc >= 0) {
+            const int par = S.lane[lk[k]].t & 1;
+            tix[k] = __ldcg(w.tokidx + pl(w, se[k] < 0 ? par : par ^ 1, lk[k]) + (se[k] & 0x7fffffff));
           }
         }
-        if (s.phase == kFin) {
-          const float fw = __ldg(g.final_w + d);
-          if (fw > -INFINITY) {
-            atomicMax(&fc_of(w, f, l)->final_key, mk_key(__fadd_rn(score, fw), d));
-            atomicAdd(&w.stats[l].finals, 1ull);
+#pragma unroll
+        for (int k = 0; k < kCB; k++) {
+          if (!v[k]) continue;
+          const int l = lk[k];
+          const SmLane& s = S.lane[l];
+          const int f = s.t;
+          const int32_t arc = key_id(key[k]);
+          const float score = key_score(key[k]);
+          if (s.need_commit) {
+            const int64_t base_new = s.cursor;   // frame f
+            const int64_t base_old = s.base_cur; // frame f-1
+            const int32_t prev = arc < 0 ? -1 : (int32_t)((se[k] < 0 ? base_new : base_old) + tix[k]);
+            const int64_t idx = base_new + pk[k];
+            if (idx < w.log_cap) w.wlog[(size_t)l * w.log_cap + idx] = make_int2(prev, arc);
+            else lane_ovf(a, l, kOvfArena);
+            if (g.has_eps) {
+              const int4 m = __ldg(g.meta + st[k]);
+              if (m.z > m.y) atomicAdd(&w.stats[l].eps, (unsigned long long)(m.z - m.y));
+            }
+          }
+          if (s.phase == kFin) {
+            const float fw = __ldg(g.final_w + st[k]);
+            if (fw > -INFINITY) {
+              atomicMax(&fc_of(w, f, l)->final_key, mk_key(__fadd_rn(score, fw), st[k]));
+              atomicAdd(&w.stats[l].finals, 1ull);
+            }
+          }
+          if (s.phase == kFin || s.phase == kPart) atomicMax(&fc_of(w, f, l)->best_key, key[k]);
+          if (s.phase == kEmit && a.ub_skip && s.has_prev && score == s.prev_max) {
+            // a best token of the frame: its arcs give an achieved end early
+            const int4 m = __ldg(g.meta + st[k]);
+            const LP* row = lpb + (int64_t)s.row * a.stride_b + (int64_t)(f - s.t0) * a.stride_t;
+            float mx = -INFINITY;
+            for (int32_t ai = m.x; ai < m.y; ai++)
+              mx = fmaxf(mx, __fadd_rn(__fadd_rn(score, __ldg(g.weight + ai)),
+                                       lp_at<LP>(row, __ldg(g.ilabel + ai))));
+            if (mx > -INFINITY) atomicMax(&fc_of(w, f, l)->maxkey, ord_f(mx));
           }
         }
-        if (s.phase == kFin || s.phase == kPart) atomicMax(&fc_of(w, f, l)->best_key, key);
       }
     }
+    prof_mark(prof, tsub, kProfCommit);
     {  // clear frame t-1's recombination entries
       const int total = S.pre_c[L];
-      for (int gi = (int)gstart; gi < total; gi += (int)gstride) {
-        const int l = find_lane(S.pre_c, L, gi);
-        const int32_t p = gi - S.pre_c[l];
-        const int par = (S.lane[l].t - 1) & 1;
-        const int32_t d = __ldcg(w.claims + ql(w, par, l) + p);
-        w.payload[pl(w, par, l) + d] = 0ull;
+      for (int g0 = blockIdx.x * kThreads * kCB + tid; g0 < total; g0 += G * kThreads * kCB) {
+        int32_t st[kCB];
+        int lk[kCB];
+        bool v[kCB];
+#pragma unroll
+        for (int k = 0; k < kCB; k++) {
+          const int gi = g0 + k * kThreads;
+          v[k] = gi < total;
+          lk[k] = v[k] ? find_lane(S.pre_c, L, gi) : 0;
+          st[k] = v[k] ? __ldcg(&w.front[ql(w, (S.lane[lk[k]].t - 1) & 1, lk[k]) + gi - S.pre_c[lk[k]]].state)
+                       : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < kCB; k++)
+          if (v[k]) w.payload[pl(w, (S.lane[lk[k]].t - 1) & 1, lk[k]) + st[k]] = 0ull;
       }
     }
     if (lat) {  // lattice records of the last step: resolve their frame-t tokens
@@ -920,8 +1115,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         *rp = rec;
       }
     }
+    prof_mark(prof, tsub, kProfClear);
     emit_tiles<0, LP>(a, S);
+    prof_mark(prof, tsub, kProfMaxTiles);
     if (!grid_sync(a, S, epoch)) return;
+    prof_mark(prof, tsub, kProfBarX);
+    prof_mark(prof, tlast, kProfCommitMax);
 
     // ================= phase Y: expand (admit + recombine); final / partial
     for (int l = tid; l < L; l += kThreads) {
@@ -948,6 +1147,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
       for (int l = tid; l < L; l += kThreads)
         if (S.lane[l].phase == kEmit) w.wl_cnt[(size_t)1 * L + l] = 0ull;
     emit_tiles<1, LP>(a, S);
+    prof_mark(prof, tsub, kProfExpTiles);
 
     // final-arc lattice records (read payload; cleared only after the loop)
     if (lat) {
@@ -961,7 +1161,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         const int32_t p = gi - S.pre_c[l];
         const SmLane& s = S.lane[l];
         const int par = s.t & 1;
-        const int32_t d = __ldcg(w.claims + ql(w, par, l) + p);
+        const int32_t d = __ldcg(&w.front[ql(w, par, l) + p].state);
         const float fw = __ldg(g.final_w + d);
         if (fw > -INFINITY) {
           const float score = key_score(__ldcg(w.payload + pl(w, par, l) + d));
@@ -1083,7 +1283,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         __syncthreads();
       }
     }
+    prof_mark(prof, tsub, kProfFinal);
     if (!grid_sync(a, S, epoch)) return;
+    prof_mark(prof, tsub, kProfBarY);
+    prof_mark(prof, tlast, kProfExpand);
 
     // ================= epsilon closure of the new frames (§5.5)
     if (g.has_eps) {
@@ -1100,6 +1303,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
       __syncthreads();
       if (S.flag && !run_closure(a, S, epoch)) return;
       for (int l = tid; l < L; l += kThreads) S.lane[l].closure = 0;
+      prof_mark(prof, tlast, kProfClosure);
+      if (blockIdx.x == 0 && tid == 0) prof[kProfSlots + tsub] = prof[kProfSlots + tlast];
     }
 
     // ================= lane bookkeeping (identical in every CTA)
@@ -1135,6 +1340,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     __syncthreads();
     if (S.any && !lattice_prune(a, S, epoch)) return;
   }
+  prof_mark(prof, tlast, kProfPrune);
 
   // ---- finished lanes: clear the last frame's recombination entries
   for (int l = 0; l < L; l++) {
@@ -1142,7 +1348,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     if (!s.done_final) continue;
     const int par = s.t & 1;
     for (int64_t p = gstart; p < s.n_cur; p += gstride) {
-      const int32_t d = __ldcg(w.claims + ql(w, par, l) + p);
+      const int32_t d = __ldcg(&w.front[ql(w, par, l) + p].state);
       w.payload[pl(w, par, l) + d] = 0ull;
     }
   }
@@ -1169,7 +1375,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
       ls.sum_m += s.sum_m;
       ls.steps = steps;
     }
-    if (tid == 0) w.bar->epochs = epoch;
+    if (tid == 0) {
+      w.bar->epochs = epoch;
+      prof_mark(prof, tlast, kProfTail);
+      for (int i = 0; i < kProfSlots; i++) w.prof[i] = prof[i];
+    }
   }
 }
 
