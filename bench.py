@@ -179,9 +179,10 @@ def run_gpu(args):
     wl = synth.workload(args.workload)
     g = synth.make_graph(args.workload)
     G = W.Graph(g, device=local)
-    params = W.make_params(wl.search_beam, wl.output_beam, wl.min_active, wl.max_active, True, False)
+    params = W.make_params(wl.search_beam, wl.output_beam, wl.min_active, wl.max_active, True, False,
+                           options=W.OPT_NO_UB_SKIP if args.no_ub_skip else 0)
     nl = args.lanes or wl.B
-    caps = W.Capacity(0, args.log_cap, 0, 0) if args.log_cap else None
+    caps = W.Capacity(args.frontier_cap, args.log_cap, 0, 0) if (args.log_cap or args.frontier_cap) else None
     D = W.Decoder(G, params, nl, wl.T, caps)
     # each rank decodes its own batch (lanes are independent: weak scaling)
     lanes = [rank * nl + b for b in range(nl)]
@@ -293,6 +294,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--lanes", type=int, default=0, help="lanes per rank (default: the workload's B)")
+    ap.add_argument("--no-ub-skip", action="store_true", help="turn off the exact upper-bound skips")
+    ap.add_argument("--frontier-cap", type=int, default=0, help="tokens per lane per frame (0: default)")
     ap.add_argument("--log-cap", type=int, default=0, help="winners-log entries per lane (0: default)")
     args = ap.parse_args()
     if args.impl == "reference":

@@ -207,6 +207,16 @@ extern "C" int wfst_graph_upload(const wfst_graph_desc* d, int32_t device, wfst_
   }
   if (e == cudaSuccess) e = dev_upload(&p_col, d->olabel, A, g->allocs, g->bytes);
   if (e == cudaSuccess) e = dev_upload(&p_fin, d->final_weight, N, g->allocs, g->bytes);
+  int4* p_arcs = nullptr;
+  if (e == cudaSuccess) {
+    std::vector<int4> rec(A ? A : 1);
+    for (int64_t k = 0; k < A; k++) {
+      int32_t wb;
+      std::memcpy(&wb, &wt[k], 4);
+      rec[k] = make_int4(dst[k], wb, il16[k] == 0xFFFF ? -1 : (int32_t)il16[k], aid[k]);
+    }
+    e = dev_upload(&p_arcs, rec.data(), A, g->allocs, g->bytes);
+  }
   if (e != cudaSuccess) {
     graph_release(g);
     return e == cudaErrorMemoryAllocation ? fail(WFST_ERR_OOM, "graph_upload: out of device memory")
@@ -221,6 +231,7 @@ extern "C" int wfst_graph_upload(const wfst_graph_desc* d, int32_t device, wfst_
   G.c_dst = p_cdst;
   G.c_olabel = p_col;
   G.final_w = p_fin;
+  G.arcs = p_arcs;
   *out = g;
   return WFST_OK;
 }
@@ -350,8 +361,8 @@ extern "C" int wfst_decoder_create(wfst_graph* g, const wfst_params* params, int
   cudaError_t e = cudaSuccess;
 #define DA(ptr, n, z) \
   if (e == cudaSuccess) e = dalloc(d, &(ptr), (size_t)(n), z)
-  DA(w.payload, 2 * L * N, true);
-  DA(w.tokidx, 2 * L * N, false);
+  DA(w.ent, 2 * L * N, true);
+  DA(w.tpos, L * N, false);
   DA(w.front, 2 * L * qcap, false);
   DA(w.score, 2 * L * qcap, false);
   DA(w.maxlp, L * (size_t)std::max(max_frames, 1), false);
@@ -520,7 +531,7 @@ static int run_call(wfst_decoder* d, const void* lp, int32_t dtype, int64_t stri
   CU(cudaStreamSynchronize(st), "decode");
   if (d->h_bar->error & 1u) {
     // the call was abandoned mid-way: every lane's state is void
-    cudaMemsetAsync(w.payload, 0, sizeof(unsigned long long) * 2 * L * (size_t)w.N, st);
+    cudaMemsetAsync(w.ent, 0, sizeof(ulonglong2) * 2 * L * (size_t)w.N, st);
     cudaStreamSynchronize(st);
     for (size_t l = 0; l < L; l++) {
       d->chan_state[l] = 0;
@@ -561,9 +572,7 @@ static int run_call(wfst_decoder* d, const void* lp, int32_t dtype, int64_t stri
 // made it into a claims list were not cleared).
 static int sanitize(wfst_decoder* d, int32_t lane, cudaStream_t st) {
   const size_t N = (size_t)d->w.N;
-  for (int par = 0; par < 2; par++)
-    CU(cudaMemsetAsync(d->w.payload + ((size_t)par * d->L + lane) * N, 0, sizeof(unsigned long long) * N, st),
-       "sanitise");
+  CU(cudaMemsetAsync(d->w.ent + (size_t)lane * N * 2, 0, sizeof(ulonglong2) * 2 * N, st), "sanitise");
   return WFST_OK;
 }
 

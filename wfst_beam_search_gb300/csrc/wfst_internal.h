@@ -44,6 +44,7 @@ struct DevGraph {
   const float* weight;            // [A] internal
   const int32_t* dst;             // [A] internal
   const int32_t* arc_id;          // [A] internal -> caller id (nullptr when identity)
+  const int4* arcs;               // [A] internal {dst, weight bits, ilabel, caller id}: expand pass
   const int32_t* c_src;           // [A] caller id -> src state | (epsilon << 31)
   const int32_t* c_dst;           // [A] caller id -> dst state
   const int32_t* c_olabel;        // [A] caller id -> olabel
@@ -125,8 +126,9 @@ struct DevWork {
   int64_t log_cap, lat_cap, path_cap;
   int64_t tiles_cap;              // tiles per lane per frame
   int32_t lattice, max_frames;
-  unsigned long long* payload;    // [2][L][N] recombination keys, 0 = empty
-  int32_t* tokidx;                // [2][L][N] position of a state in its frame
+  ulonglong2* ent;                // [L][N][2] recombination entries, 16 bytes per state and frame
+                                  // parity: {key, src}; 0 = empty (see the kernel)
+  int2* tpos;                     // [L][N] position of a state's token in its frame, per parity
   TokRec* front;                  // [2][L][qcap] tokens of a frame (the frontier), claim order
   float* score;                   // [2][L][qcap] token scores, staged by the max pass
   int32_t* tile_first;            // [2][L][tiles_cap] token holding each tile's first slot

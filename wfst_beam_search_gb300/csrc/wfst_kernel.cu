@@ -59,6 +59,7 @@ struct WStage {                   // one warp's staged tokens of its current til
   float score[kTokCap];
   int32_t state[kTokCap];
   float ub[kTokCap];
+  int32_t tpos[kTokCap];          // epsilon worklists: the token's position in its frame
 };
 
 struct Smem {
@@ -111,6 +112,9 @@ __device__ __forceinline__ unsigned lanemask_lt() {
   unsigned m;
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
   return m;
+}
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" : : "l"(p));
 }
 __device__ __forceinline__ TokRec ld_tok(const TokRec* p) {
   const int4 v = __ldcg(reinterpret_cast<const int4*>(p));
@@ -245,7 +249,7 @@ __device__ __forceinline__ void lane_ovf(const RunArgs& a, int l, int bits) {
 }
 
 __device__ __forceinline__ size_t pl(const DevWork& w, int par, int l) {
-  return ((size_t)par * w.L + l) * (size_t)w.N;       // payload / tokidx row
+  return ((size_t)par * w.L + l) * (size_t)w.N;       // per-state arrays of a lane (marks)
 }
 __device__ __forceinline__ size_t ql(const DevWork& w, int par, int l) {
   return ((size_t)par * w.L + l) * (size_t)w.qcap;    // front / score / worklists
@@ -255,6 +259,61 @@ __device__ __forceinline__ size_t tl(const DevWork& w, int par, int l) {
 }
 __device__ __forceinline__ FrameCnt* fc_of(const DevWork& w, int f, int l) {
   return w.fcnt + (size_t)(f & 3) * w.L + l;
+}
+
+// Recombination entry of state d, lane l, frame parity par: 16 bytes
+// {key, src} where key = (ordered score, 0x7fffffff - arc id) of the best
+// incoming candidate so far and src = the position of that candidate's source
+// token (in the previous frame for an emitting arc; in the same frame, with
+// bit 31 set, for an epsilon arc).  Both parities of a state share one
+// 32-byte sector, so a state that stays in the frontier keeps hitting the
+// same line frame after frame.  The token's own position lives in tpos.
+__device__ __forceinline__ ulonglong2* ent_at(const DevWork& w, int l, int32_t d, int par) {
+  return w.ent + ((((size_t)l * (size_t)w.N + (size_t)d) << 1) | (size_t)par);
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const void* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ ulonglong2 cas128(ulonglong2* p, ulonglong2 cmp, ulonglong2 val) {
+  ulonglong2 old;
+  asm volatile(
+      "{\n\t.reg .b128 c, v, o;\n\t"
+      "mov.b128 c, {%2, %3};\n\t"
+      "mov.b128 v, {%4, %5};\n\t"
+      "atom.relaxed.gpu.global.cas.b128 o, [%6], c, v;\n\t"
+      "mov.b128 {%0, %1}, o;\n\t}"
+      : "=l"(old.x), "=l"(old.y)
+      : "l"(cmp.x), "l"(cmp.y), "l"(val.x), "l"(val.y), "l"(p)
+      : "memory");
+  return old;
+}
+
+constexpr int kCasTries = 1 << 16;  // a CAS retry only follows another thread's progress
+
+// Offer a candidate: 2 = claimed the empty entry, 1 = improved it, 0 = no change.
+// The first attempt assumes an empty entry (the common case for a new
+// state), so a claim costs one round trip; a failed CAS returns the current
+// value and the loop continues from it.
+__device__ __forceinline__ int relax_ent(const RunArgs& a, ulonglong2* e, unsigned long long key, uint32_t src) {
+  ulonglong2 cur = make_ulonglong2(0ull, 0ull);
+  const ulonglong2 nv = make_ulonglong2(key, (unsigned long long)src);
+  for (int it = 0; it < kCasTries; it++) {
+    if (key <= cur.x) return 0;
+    const ulonglong2 old = cas128(e, cur, nv);
+    if (old.x == cur.x && old.y == cur.y) return cur.x == 0ull ? 2 : 1;
+    cur = old;
+  }
+  atomicOr(&a.w.bar->error, 4u);
+  return 0;
+}
+
+__device__ __forceinline__ uint32_t ent_src(const ulonglong2& e) { return (uint32_t)e.y; }
+__device__ __forceinline__ int32_t* tpos_at(const DevWork& w, int l, int32_t d, int par) {
+  return reinterpret_cast<int32_t*>(w.tpos + ((size_t)l * (size_t)w.N + (size_t)d)) + par;
 }
 
 __device__ __forceinline__ uint32_t warp_inc_scan(uint32_t v) {
@@ -276,7 +335,7 @@ __device__ __forceinline__ uint32_t warp_inc_scan(uint32_t v) {
 template <int K, bool EPS>
 __device__ __forceinline__ void warp_append(const bool (&want)[K], const int32_t (&d)[K],
                                             unsigned long long* ctr, TokRec* list, int32_t* tfirst,
-                                            int32_t* tokidx, int64_t cap, const RunArgs& a, int l) {
+                                            int pos_par, int64_t cap, const RunArgs& a, int l) {
   const unsigned full = 0xffffffffu;
   uint32_t cnt_sum = 0, tot_sum = 0;
 #pragma unroll
@@ -309,7 +368,7 @@ __device__ __forceinline__ void warp_append(const bool (&want)[K], const int32_t
       const uint32_t off = ob + inc - dv;
       if (p < (uint64_t)cap) {
         *reinterpret_cast<int4*>(list + p) = make_int4(d[k], (int)off, EPS ? md.y : md.x, EPS ? 0 : md.w);
-        if (tokidx) tokidx[d[k]] = (int32_t)p;
+        if (pos_par >= 0) *tpos_at(a.w, l, d[k], pos_par) = (int32_t)p;
         if (dv > 0) {
           const uint32_t k0 = (off + kTile - 1) / kTile, k1 = (off + dv - 1) / kTile;
           for (uint32_t q = k0; q <= k1; q++) tfirst[q] = (int32_t)p;
@@ -331,7 +390,7 @@ __device__ __forceinline__ void warp_claim(const RunArgs& a, const bool (&want)[
   const DevWork& w = a.w;
   const int par = f & 1;
   warp_append<K, false>(want, d, &fc_of(w, f, l)->cnt, w.front + ql(w, par, l), w.tile_first + tl(w, par, l),
-                        w.tokidx + pl(w, par, l), w.qcap, a, l);
+                        par, w.qcap, a, l);
   if (a.g.has_eps && seed_worklist) {
     bool ws[K];
 #pragma unroll
@@ -342,7 +401,7 @@ __device__ __forceinline__ void warp_claim(const RunArgs& a, const bool (&want)[
         ws[k] = m.z > m.y;
       }
     }
-    warp_append<K, true>(ws, d, &w.wl_cnt[l], w.wl + ql(w, 0, l), w.wl_tile_first + tl(w, 0, l), nullptr,
+    warp_append<K, true>(ws, d, &w.wl_cnt[l], w.wl + ql(w, 0, l), w.wl_tile_first + tl(w, 0, l), -1,
                          w.qcap, a, l);
   }
 }
@@ -394,7 +453,6 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
     if (p_hi > s.n_cur) p_hi = s.n_cur;
     const LP* row = lpb + (int64_t)s.row * a.stride_b + (int64_t)(f - s.t0) * a.stride_t;
     const size_t q = ql(w, par, l);
-    const size_t pay = pl(w, par, l);
     const float maxlp = s.maxlp;
     // the skip threshold: an end already achieved (max) / the cutoff (expand)
     float thr = s.cutoff;
@@ -415,7 +473,7 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
           const TokRec tr = ld_tok(w.front + q + c + i);
           float sc;
           if (MODE == 0) {
-            sc = key_score(__ldcg(w.payload + pay + tr.state));
+            sc = key_score(__ldcg(&ent_at(w, l, tr.state, par)->x));
             w.score[q + c + i] = sc;
           } else {
             sc = __ldcg(w.score + q + c + i);
@@ -442,12 +500,24 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
         if (act[j] && a.ub_skip && ws.ub[ti[j]] <= thr) act[j] = false;
         ai[j] = act[j] ? ws.row[ti[j]] + (int32_t)(slot - ws.off[ti[j]]) : 0;
       }
+      // the max pass reads the ilabel/weight columns; the expand pass reads one
+      // 16-byte record per arc {dst, weight, ilabel, arc id} (one vector load)
       int il[kSPT];
       float wt[kSPT];
+      int32_t d[kSPT], id[kSPT];
 #pragma unroll
       for (int j = 0; j < kSPT; j++) {
-        il[j] = act[j] ? (int)__ldg(g.ilabel + ai[j]) : 0;
-        wt[j] = act[j] ? __ldg(g.weight + ai[j]) : 0.f;
+        if (MODE == 0) {
+          il[j] = act[j] ? (int)__ldg(g.ilabel + ai[j]) : 0;
+          wt[j] = act[j] ? __ldg(g.weight + ai[j]) : 0.f;
+          d[j] = id[j] = 0;
+        } else {
+          const int4 r = act[j] ? __ldg(g.arcs + ai[j]) : make_int4(0, 0, 0, 0);
+          d[j] = r.x;
+          wt[j] = __int_as_float(r.y);
+          il[j] = r.z;
+          id[j] = r.w;
+        }
       }
       float end[kSPT];
 #pragma unroll
@@ -460,14 +530,11 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
 #pragma unroll
         for (int j = 0; j < kSPT; j++) vmax = fmaxf(vmax, end[j]);
       } else {
-        const size_t npay = pl(w, par ^ 1, l);
         bool adm[kSPT], claim[kSPT];
-        int32_t d[kSPT], id[kSPT];
 #pragma unroll
         for (int j = 0; j < kSPT; j++) {
           adm[j] = act[j] && (end[j] > thr);
-          d[j] = adm[j] ? __ldg(g.dst + ai[j]) : 0;
-          id[j] = adm[j] ? (g.identity ? ai[j] : __ldg(g.arc_id + ai[j])) : 0;
+          if (!adm[j]) d[j] = id[j] = 0;
         }
         if (a.lattice) {
 #pragma unroll
@@ -486,7 +553,8 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
         }
 #pragma unroll
         for (int j = 0; j < kSPT; j++) {
-          claim[j] = adm[j] && atomicMax(w.payload + npay + d[j], mk_key(end[j], id[j])) == 0ull;
+          claim[j] = adm[j] && relax_ent(a, ent_at(w, l, d[j], par ^ 1), mk_key(end[j], id[j]),
+                                         (uint32_t)(c + ti[j])) == 2;
           admitted += adm[j] ? 1u : 0u;
         }
         warp_claim<kSPT>(a, claim, d, l, f + 1, true);
@@ -529,7 +597,6 @@ __device__ void eps_tiles(const RunArgs& a, Smem& S, int buf, int next_slot) {
     if (p_hi > s.wl_n) p_hi = s.wl_n;
     const float cutoff = s.cutoff;
     const size_t q = ql(w, buf, l);
-    const size_t pay = pl(w, par, l);
     const uint32_t pass_id = s.eps_pass + 1;
     for (int32_t c = p_lo; c < p_hi; c += kTokCap) {
       const int ntok = min(kTokCap, p_hi - c);
@@ -541,7 +608,8 @@ __device__ void eps_tiles(const RunArgs& a, Smem& S, int buf, int next_slot) {
           const TokRec tr = ld_tok(w.wl + q + c + i);
           ws.off[i] = tr.off;
           ws.row[i] = tr.row;  // first epsilon arc
-          ws.score[i] = key_score(__ldcg(w.payload + pay + tr.state));
+          ws.score[i] = key_score(__ldcg(&ent_at(w, l, tr.state, par)->x));
+          ws.tpos[i] = __ldcg(tpos_at(w, l, tr.state, par));
           ws.state[i] = tr.state;
         }
       }
@@ -563,13 +631,17 @@ __device__ void eps_tiles(const RunArgs& a, Smem& S, int buf, int next_slot) {
       bool adm[kSPT];
       int32_t d[kSPT], id[kSPT];
 #pragma unroll
-      for (int j = 0; j < kSPT; j++) wt[j] = act[j] ? __ldg(g.weight + ai[j]) : 0.f;
+      for (int j = 0; j < kSPT; j++) {
+        const int4 r = act[j] ? __ldg(g.arcs + ai[j]) : make_int4(0, 0, 0, 0);
+        d[j] = r.x;
+        wt[j] = __int_as_float(r.y);
+        id[j] = r.w;
+      }
 #pragma unroll
       for (int j = 0; j < kSPT; j++) {
         e[j] = __fadd_rn(ws.score[ti[j]], wt[j]);
         adm[j] = act[j] && (e[j] > cutoff);
-        d[j] = adm[j] ? __ldg(g.dst + ai[j]) : 0;
-        id[j] = adm[j] ? (g.identity ? ai[j] : __ldg(g.arc_id + ai[j])) : 0;
+        if (!adm[j]) d[j] = id[j] = 0;
       }
       if (a.lattice) {
 #pragma unroll
@@ -589,10 +661,11 @@ __device__ void eps_tiles(const RunArgs& a, Smem& S, int buf, int next_slot) {
       bool claim[kSPT], better[kSPT];
 #pragma unroll
       for (int j = 0; j < kSPT; j++) {
-        const unsigned long long key = mk_key(e[j], id[j]);
-        const unsigned long long old = adm[j] ? atomicMax(w.payload + pay + d[j], key) : ~0ull;
-        claim[j] = adm[j] && old == 0ull;
-        better[j] = adm[j] && key > old;
+        const int r = adm[j] ? relax_ent(a, ent_at(w, l, d[j], par), mk_key(e[j], id[j]),
+                                         0x80000000u | (uint32_t)ws.tpos[ti[j]])
+                             : 0;
+        claim[j] = r == 2;
+        better[j] = r >= 1;
       }
       warp_claim<kSPT>(a, claim, d, l, fr, false);
       bool wl[kSPT];
@@ -605,7 +678,7 @@ __device__ void eps_tiles(const RunArgs& a, Smem& S, int buf, int next_slot) {
         }
       }
       warp_append<kSPT, true>(wl, d, &w.wl_cnt[(size_t)next_slot * L + l], w.wl + ql(w, buf ^ 1, l),
-                              w.wl_tile_first + tl(w, buf ^ 1, l), nullptr, w.qcap, a, l);
+                              w.wl_tile_first + tl(w, buf ^ 1, l), -1, w.qcap, a, l);
     }
   }
 }
@@ -672,9 +745,9 @@ __device__ void init_lane_global(const RunArgs& a, int l) {
   const int32_t s0 = g.start;
   const int4 m = __ldg(g.meta + s0);
   const uint32_t deg = (uint32_t)(m.y - m.x);
-  w.payload[pl(w, 0, l) + s0] = mk_key(0.0f, -1);
+  *ent_at(w, l, s0, 0) = make_ulonglong2(mk_key(0.0f, -1), 0ull);
+  *tpos_at(w, l, s0, 0) = 0;
   *reinterpret_cast<int4*>(w.front + ql(w, 0, l)) = make_int4(s0, 0, m.x, m.w);
-  w.tokidx[pl(w, 0, l) + s0] = 0;
   if (deg > 0)
     for (uint32_t k = 0; k <= (deg - 1) / kTile; k++) w.tile_first[tl(w, 0, l) + k] = 0;
   w.fcnt[l].cnt = (1ull << 32) | deg;
@@ -1014,24 +1087,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
           pk[k] = v[k] ? gi - S.pre_b[lk[k]] : 0;
           st[k] = v[k] ? __ldcg(&w.front[ql(w, S.lane[lk[k]].t & 1, lk[k]) + pk[k]].state) : 0;
         }
-#pragma unroll
-        for (int k = 0; k < kCB; k++)
-          key[k] = v[k] ? __ldcg(w.payload + pl(w, S.lane[lk[k]].t & 1, lk[k]) + st[k]) : 0ull;
-        int32_t se[kCB];
+        uint32_t src[kCB];
 #pragma unroll
         for (int k = 0; k < kCB; k++) {
-          const int32_t arc = key_id(key[k]);
-          se[k] = (v[k] && S.lane[lk[k]].need_commit && arc >= 0) ? __ldg(g.c_src + arc) : 0;
-        }
-        int32_t tix[kCB];
-#pragma unroll
-        for (int k = 0; k < kCB; k++) {
-          const int32_t arc = key_id(key[k]);
-          tix[k] = 0;
-          if (v[k] && S.lane[lk[k]].need_commit && arc >= 0) {
-            const int par = S.lane[lk[k]].t & 1;
-            tix[k] = __ldcg(w.tokidx + pl(w, se[k] < 0 ? par : par ^ 1, lk[k]) + (se[k] & 0x7fffffff));
-          }
+          const ulonglong2 e = v[k] ? __ldcg(ent_at(w, lk[k], st[k], S.lane[lk[k]].t & 1)) : make_ulonglong2(0, 0);
+          key[k] = e.x;
+          src[k] = ent_src(e);
         }
 #pragma unroll
         for (int k = 0; k < kCB; k++) {
@@ -1044,7 +1105,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
           if (s.need_commit) {
             const int64_t base_new = s.cursor;   // frame f
             const int64_t base_old = s.base_cur; // frame f-1
-            const int32_t prev = arc < 0 ? -1 : (int32_t)((se[k] < 0 ? base_new : base_old) + tix[k]);
+            // the winner's source token: same frame for an epsilon arc, else the previous one
+            const int32_t prev =
+                arc < 0 ? -1 : (int32_t)(((src[k] >> 31) ? base_new : base_old) + (src[k] & 0x7fffffffu));
             const int64_t idx = base_new + pk[k];
             if (idx < w.log_cap) w.wlog[(size_t)l * w.log_cap + idx] = make_int2(prev, arc);
             else lane_ovf(a, l, kOvfArena);
@@ -1091,7 +1154,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         }
 #pragma unroll
         for (int k = 0; k < kCB; k++)
-          if (v[k]) w.payload[pl(w, (S.lane[lk[k]].t - 1) & 1, lk[k]) + st[k]] = 0ull;
+          if (v[k]) *ent_at(w, lk[k], st[k], (S.lane[lk[k]].t - 1) & 1) = make_ulonglong2(0ull, 0ull);
       }
     }
     if (lat) {  // lattice records of the last step: resolve their frame-t tokens
@@ -1104,12 +1167,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         LatRec rec = *rp;
         const int par = s.t & 1;
         const int64_t base_new = s.cursor;  // frame t
-        rec.dst_tok = (int32_t)(base_new + __ldcg(w.tokidx + pl(w, par, l) + rec.dst_state));
+        rec.dst_tok = (int32_t)(base_new + __ldcg(tpos_at(w, l, rec.dst_state, par)));
         if (rec.frame_flags & kRecEps) {
           // keep only the relaxation evaluated with the source's final score
           const unsigned used = (unsigned)rec.src_tok;
-          const float fin = key_score(__ldcg(w.payload + pl(w, par, l) + rec.src_state));
-          rec.src_tok = (int32_t)(base_new + __ldcg(w.tokidx + pl(w, par, l) + rec.src_state));
+          const float fin = key_score(__ldcg(&ent_at(w, l, rec.src_state, par)->x));
+          rec.src_tok = (int32_t)(base_new + __ldcg(tpos_at(w, l, rec.src_state, par)));
           if (ord_f(__uint_as_float(used)) != ord_f(fin)) rec.frame_flags |= kRecDead;
         }
         *rp = rec;
@@ -1149,7 +1212,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     emit_tiles<1, LP>(a, S);
     prof_mark(prof, tsub, kProfExpTiles);
 
-    // final-arc lattice records (read payload; cleared only after the loop)
+    // final-arc lattice records (read the entries; cleared only after the loop)
     if (lat) {
       for (int l = tid; l < L; l += kThreads)
         S.pre_c[l] = (S.lane[l].phase == kFin) ? S.lane[l].n_cur : 0;
@@ -1164,7 +1227,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         const int32_t d = __ldcg(&w.front[ql(w, par, l) + p].state);
         const float fw = __ldg(g.final_w + d);
         if (fw > -INFINITY) {
-          const float score = key_score(__ldcg(w.payload + pl(w, par, l) + d));
+          const float score = key_score(__ldcg(&ent_at(w, l, d, par)->x));
           LatRec r;
           r.frame_flags = (s.t << 4) | kRecFinal;
           r.src_tok = (int32_t)(s.base_cur + p);
@@ -1212,7 +1275,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
           }
           if (__ldcg(&w.lanes[l].overflow) & kOvfArena) ok = 0;
           int64_t idx = -1;
-          if (ok) idx = s.base_cur + __ldcg(w.tokidx + pl(w, par, l) + state);
+          if (ok) idx = s.base_cur + __ldcg(tpos_at(w, l, state, par));
           // walk the winners chain; the newest arc lands at the end of the buffer
           int64_t n = 0;
           int32_t* path = w.path + (size_t)l * w.path_cap;
@@ -1349,7 +1412,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     const int par = s.t & 1;
     for (int64_t p = gstart; p < s.n_cur; p += gstride) {
       const int32_t d = __ldcg(&w.front[ql(w, par, l) + p].state);
-      w.payload[pl(w, par, l) + d] = 0ull;
+      *ent_at(w, l, d, par) = make_ulonglong2(0ull, 0ull);
     }
   }
 
