@@ -229,6 +229,34 @@ int wfst_stream_release(wfst_decoder* d, int32_t channel);
 #define WFST_STAT_COUNT 23
 int wfst_stats(wfst_decoder* d, int64_t* out, int32_t n);
 
+/*
+ * Offline decode that allocates nothing (no device or pinned memory, no
+ * decoder object).  "GPU WFST Beam-Search Decoder" has no counterpart: its
+ * decoder sizes a workspace per decoder (§6.1).  This is the same decode as wfst_decode for
+ * callers that may not allocate once running (their own memory pool, a
+ * real-time thread): its working memory is one region of
+ * WFST_STATIC_SCRATCH_BYTES that the library declares statically, one per
+ * device per process.
+ * Arguments as in wfst_decode, with the decoder replaced by the graph and
+ * its params: lattice and streaming must be 0; log_probs must be device
+ * memory on the graph's device; B <= WFST_STATIC_MAX_LANES; frontier and
+ * log capacities are never exceeded (frontier = num_states).
+ * The first call on a device resolves the region's address and may load the
+ * module there: make it before any stream capture begins.  The zero-start
+ * part of the region (entries, marks, counters, barrier, results) is cleared
+ * by every call.  Calls on one device are serialized by a lock held until
+ * the results are on the host: calls that overlapped would race on the
+ * region.
+ * Errors: INVALID_ARG, CAPACITY (B or the call's tables exceed the region;
+ * the message gives the bytes needed), CUDA, TIMEOUT.
+ */
+#define WFST_STATIC_SCRATCH_BYTES (16u << 20)
+#define WFST_STATIC_MAX_LANES 8
+int wfst_decode_static(const wfst_graph* g, const wfst_params* params, const void* log_probs,
+                       int32_t dtype, int64_t stride_b, int64_t stride_t, const int32_t* lens,
+                       int32_t B, int32_t T, void* stream, int32_t* words, int32_t words_cap,
+                       int32_t* word_lens, double* scores, int32_t* meta);
+
 const char* wfst_last_error(void);
 
 #ifdef __cplusplus

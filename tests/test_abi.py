@@ -52,6 +52,8 @@ def test_last_error_and_argument_checks_without_gpu(lib):
     assert lib.wfst_graph_upload(None, 0, None) == -1
     assert b"NULL" in lib.wfst_last_error()
     assert lib.wfst_decode(None, None, 0, 0, 0, None, 0, 0, None, None, 0, None, None, None) == -1
+    assert lib.wfst_decode_static(None, None, None, 0, 0, 0, None, 0, 0, None, None, 0, None, None,
+                                  None) == -1
 
 
 def test_graph_validation_rejects_corrupt_graphs_on_host(lib):

@@ -36,7 +36,7 @@ LAT_DTYPE = np.dtype([("t", "<i4"), ("src_state", "<i4"), ("dst_state", "<i4"),
 EXPORTED = ["wfst_graph_upload", "wfst_graph_info", "wfst_graph_free", "wfst_decoder_create",
             "wfst_decoder_free", "wfst_decode", "wfst_lattice_export", "wfst_stream_create",
             "wfst_stream_advance", "wfst_stream_finalize", "wfst_stream_release", "wfst_stats",
-            "wfst_last_error"]
+            "wfst_decode_static", "wfst_last_error"]
 
 
 class WfstError(RuntimeError):
@@ -95,6 +95,8 @@ def load(build_if_missing: bool = False):
         L.wfst_decoder_free.argtypes = [P]
         L.wfst_decoder_free.restype = None
         L.wfst_decode.argtypes = [P, P, i32, i64, i64, P, i32, i32, P, P, i32, P, P, P]
+        L.wfst_decode_static.argtypes = [P, C.POINTER(Params), P, i32, i64, i64, P, i32, i32, P, P,
+                                         i32, P, P, P]
         L.wfst_lattice_export.argtypes = [P, i32, P, i64, C.POINTER(i64)]
         L.wfst_stream_create.argtypes = [P, C.POINTER(i32)]
         L.wfst_stream_advance.argtypes = [P, P, i32, P, i32, i64, i64, P, i32, i32, P, P, i32, P,
@@ -159,6 +161,29 @@ def wfst_decode(h, lp_ptr, dtype, stride_b, stride_t, lens_ptr, B, T, stream, wo
                 words_cap, word_lens_ptr, scores_ptr, meta_ptr):
     _check(load().wfst_decode(h, lp_ptr, dtype, stride_b, stride_t, lens_ptr, B, T, stream,
                               words_ptr, words_cap, word_lens_ptr, scores_ptr, meta_ptr))
+
+
+def wfst_decode_static(graph_h, params, lp_ptr, dtype, stride_b, stride_t, lens_ptr, B, T, stream,
+                       words_ptr, words_cap, word_lens_ptr, scores_ptr, meta_ptr):
+    _check(load().wfst_decode_static(graph_h, C.byref(params), lp_ptr, dtype, stride_b, stride_t,
+                                     lens_ptr, B, T, stream, words_ptr, words_cap, word_lens_ptr,
+                                     scores_ptr, meta_ptr))
+
+
+def decode_static(graph, params, lp, lens, stream=None, words_cap=4096):
+    """Offline decode through ``wfst_decode_static`` (no allocation by the
+    library; ``lp`` must be a CUDA tensor on the graph's device, B <= 8)."""
+    ptr, dt, sb, st, B, T = _lp_args(lp)
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    words = np.zeros((B, max(words_cap, 1)), np.int32)
+    wl = np.zeros(B, np.int32)
+    sc = np.zeros(B, np.float64)
+    meta = np.zeros((B, 3), np.int32)
+    wfst_decode_static(graph.h, params, ptr, dt, sb, st, _ptr(lens), B, T, _stream(stream),
+                       _ptr(words), words_cap, _ptr(wl), _ptr(sc), _ptr(meta))
+    return [dict(words=words[b, : min(wl[b], words_cap)].copy(), n_words=int(wl[b]),
+                 score=float(sc[b]), ok=int(meta[b, 0]), reached_final=int(meta[b, 1]),
+                 overflow=int(meta[b, 2])) for b in range(B)]
 
 
 def wfst_lattice_export(h, lane, out_ptr, cap):

@@ -251,6 +251,16 @@ extern "C" int wfst_graph_info(const wfst_graph* g, int64_t* out) {
 
 extern "C" void wfst_graph_free(wfst_graph* g) { graph_release(g); }
 
+// Accessors for the other host translation unit (wfst_static.cu).
+namespace wfst {
+int api_fail(int code, const char* msg) { return fail(code, msg); }
+int api_cuda_fail(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+const DevGraph* api_graph(const wfst_graph* g, int* device) {
+  *device = g->device;
+  return &g->dg;
+}
+}  // namespace wfst
+
 // ---------------------------------------------------------------------------- decoder
 
 struct wfst_decoder {
