@@ -312,6 +312,11 @@ __device__ __forceinline__ int relax_ent(const RunArgs& a, ulonglong2* e, unsign
 }
 
 __device__ __forceinline__ uint32_t ent_src(const ulonglong2& e) { return (uint32_t)e.y; }
+// Token positions per state are kept only where something looks a state's
+// token up (epsilon worklists, lattice records); the final backtrack of other
+// graphs finds its one token by a scan of the frame.
+__device__ __forceinline__ bool tpos_kept(const RunArgs& a) { return a.g.has_eps || a.lattice; }
+
 __device__ __forceinline__ int32_t* tpos_at(const DevWork& w, int l, int32_t d, int par) {
   return reinterpret_cast<int32_t*>(w.tpos + ((size_t)l * (size_t)w.N + (size_t)d)) + par;
 }
@@ -390,7 +395,7 @@ __device__ __forceinline__ void warp_claim(const RunArgs& a, const bool (&want)[
   const DevWork& w = a.w;
   const int par = f & 1;
   warp_append<K, false>(want, d, &fc_of(w, f, l)->cnt, w.front + ql(w, par, l), w.tile_first + tl(w, par, l),
-                        par, w.qcap, a, l);
+                        tpos_kept(a) ? par : -1, w.qcap, a, l);
   if (a.g.has_eps && seed_worklist) {
     bool ws[K];
 #pragma unroll
@@ -1074,7 +1079,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     {  // commit (§5.4): winners-log entry {prev, arc} per token; final-step
        // keys; a best token of an emitting lane seeds the exact max
       const int total = S.pre_b[L];
-      for (int g0 = blockIdx.x * kThreads * kCB + tid; g0 < total; g0 += G * kThreads * kCB) {
+      const int wlane = tid & 31;
+      // warp-uniform trip count: the seed below is a warp-collective
+      for (int wb = blockIdx.x * kThreads * kCB + (tid & ~31); wb < total; wb += G * kThreads * kCB) {
+        const int g0 = wb + wlane;
+        unsigned seed = 0;  // bit k: token k of this thread seeds the max
         int lk[kCB];
         int32_t pk[kCB], st[kCB];
         bool v[kCB];
@@ -1124,15 +1133,29 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
             }
           }
           if (s.phase == kFin || s.phase == kPart) atomicMax(&fc_of(w, f, l)->best_key, key[k]);
-          if (s.phase == kEmit && a.ub_skip && s.has_prev && score == s.prev_max) {
-            // a best token of the frame: its arcs give an achieved end early
-            const int4 m = __ldg(g.meta + st[k]);
-            const LP* row = lpb + (int64_t)s.row * a.stride_b + (int64_t)(f - s.t0) * a.stride_t;
+          if (s.phase == kEmit && a.ub_skip && s.has_prev && score == s.prev_max) seed |= 1u << k;
+        }
+        // a best token of the frame: its arcs give an achieved end early; the
+        // warp walks them together
+#pragma unroll
+        for (int k = 0; k < kCB; k++) {
+          unsigned m32 = __ballot_sync(0xffffffffu, (seed >> k) & 1u);
+          while (m32) {
+            const int src = __ffs(m32) - 1;
+            m32 &= m32 - 1;
+            const int l = __shfl_sync(0xffffffffu, lk[k], src);
+            const int32_t state = __shfl_sync(0xffffffffu, st[k], src);
+            const float score = __shfl_sync(0xffffffffu, key_score(key[k]), src);
+            const SmLane& s = S.lane[l];
+            const int4 m = __ldg(g.meta + state);
+            const LP* row = lpb + (int64_t)s.row * a.stride_b + (int64_t)(s.t - s.t0) * a.stride_t;
             float mx = -INFINITY;
-            for (int32_t ai = m.x; ai < m.y; ai++)
+            for (int32_t ai = m.x + wlane; ai < m.y; ai += 32)
               mx = fmaxf(mx, __fadd_rn(__fadd_rn(score, __ldg(g.weight + ai)),
                                        lp_at<LP>(row, __ldg(g.ilabel + ai))));
-            if (mx > -INFINITY) atomicMax(&fc_of(w, f, l)->maxkey, ord_f(mx));
+#pragma unroll
+            for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            if (wlane == 0 && mx > -INFINITY) atomicMax(&fc_of(w, s.t, l)->maxkey, ord_f(mx));
           }
         }
       }
@@ -1274,8 +1297,29 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
             score = key_score(bk);
           }
           if (__ldcg(&w.lanes[l].overflow) & kOvfArena) ok = 0;
+          S.bt_ok = ok;
+          S.bt_reached = reached;
+          S.bt_state = state;
+          S.bt_score = score;
+          S.bt_n = -1;   // the token's position in frame f, when kept
+          S.bt_pad = -1; // ... else found by the scan below
+          if (ok && tpos_kept(a)) S.bt_n = __ldcg(tpos_at(w, l, state, par));
+        }
+        __syncthreads();
+        if (S.bt_ok && S.bt_n < 0) {
+          // positions are not kept for this graph: find the state in the frame
+          for (int i = tid; i < s.n_cur; i += kThreads)
+            if (__ldcg(&w.front[ql(w, par, l) + i].state) == S.bt_state) S.bt_pad = i;
+          __syncthreads();
+        }
+        if (tid == 0) {
+          int ok = S.bt_ok;
+          const int reached = S.bt_reached, state = S.bt_state;
+          const float score = S.bt_score;
+          const int32_t pos = S.bt_n >= 0 ? S.bt_n : S.bt_pad;
+          if (pos < 0) ok = 0;
           int64_t idx = -1;
-          if (ok) idx = s.base_cur + __ldcg(tpos_at(w, l, state, par));
+          if (ok) idx = s.base_cur + pos;
           // walk the winners chain; the newest arc lands at the end of the buffer
           int64_t n = 0;
           int32_t* path = w.path + (size_t)l * w.path_cap;
