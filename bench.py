@@ -17,6 +17,7 @@ host buffers, and the CPU oracle's throughput on a bounded sample.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -34,6 +35,28 @@ import synth  # noqa: E402
 # SURVEY-defined algorithmic bytes per lane-step (n: frontier, D: emitting
 # arcs, a: admitted candidates, m: next frontier), plus one log-prob row.
 BYTES_N, BYTES_D, BYTES_A, BYTES_M = 20, 6, 16, 32
+
+
+# DRAM bytes (read + write) of one decode launch of this bench's default
+# command, from a one-pass ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum; the command is in profiles/).  It describes only the
+# kernel source it was taken on: any change to that source makes it null.
+MEASURED_TRAFFIC = {"kernel_sha256": None, "workload": "hlg-B64xT500xV5000-f16", "lanes": 64, "bytes": None}
+
+
+def kernel_sha256():
+    h = hashlib.sha256()
+    for f in ("wfst_kernel.cu", "wfst_internal.h"):
+        with open(os.path.join(ROOT, "wfst_beam_search_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload, lanes):
+    m = MEASURED_TRAFFIC
+    if m["bytes"] is None or m["workload"] != workload or m["lanes"] != lanes:
+        return None
+    return m["bytes"] if m["kernel_sha256"] == kernel_sha256() else None
 
 
 def algorithmic_bytes(st, V, esz):
@@ -105,6 +128,30 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def rank_lanes(rank: int, lanes_per_rank: int) -> list:
+    """Lanes (utterance indices) decoded by one rank: ranks take disjoint,
+    consecutive blocks, so the job decodes ranks x lanes_per_rank utterances."""
+    return [rank * lanes_per_rank + b for b in range(lanes_per_rank)]
+
+
+def reduce_over_ranks(dist, device, maxed, summed):
+    """(max over ranks of `maxed`, sum over ranks of `summed`): the job's time
+    is its slowest rank; its work is every rank's units."""
+    import torch
+    if dist is None:
+        return list(maxed), list(summed)
+    a = torch.tensor(list(maxed), device=device, dtype=torch.float64)
+    b = torch.tensor(list(summed), device=device, dtype=torch.float64)
+    dist.all_reduce(a, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return [float(x) for x in a], [float(x) for x in b]
+
+
+def job_rate(units: float, seconds: float) -> float:
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    return units / seconds
 
 
 def workload_name(wl):
@@ -185,9 +232,9 @@ def run_gpu(args):
     caps = W.Capacity(args.frontier_cap, args.log_cap, 0, 0) if (args.log_cap or args.frontier_cap) else None
     D = W.Decoder(G, params, nl, wl.T, caps)
     # each rank decodes its own batch (lanes are independent: weak scaling)
-    lanes = [rank * nl + b for b in range(nl)]
+    lanes = rank_lanes(rank, nl)
     lp_host = np.stack([synth.make_lane_log_probs(args.workload, b) for b in lanes])
-    lens = synth.make_lens(args.workload)[:nl] if nl <= wl.B else np.full(nl, wl.T, np.int32)
+    lens = synth.make_lens(args.workload)[np.asarray(lanes) % wl.B]
     esz = lp_host.itemsize
     lp_dev = torch.from_numpy(lp_host).to(dev)
     lp_pin = torch.from_numpy(lp_host).pin_memory()
@@ -222,6 +269,8 @@ def run_gpu(args):
         stats.append(s)
     ev1.record(stream)
     torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
     ms = ev0.elapsed_time(ev1)
     # end to end through the C ABI with pinned host buffers (H2D inside the call)
     pin_ptr = W._ptr(lp_pin)
@@ -231,15 +280,13 @@ def run_gpu(args):
         step(pin_ptr)
     e2e_s = time.perf_counter() - t0
     clk = clocks.stop()
-    if dist:
-        t = torch.tensor([ms, e2e_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_s = float(t[0]), float(t[1])
     frames_step = int(lens.sum())
     st0 = stats[0]
     assert all(s["frames"] == st0["frames"] and s["arcs_expanded"] == st0["arcs_expanded"] for s in stats)
-    value = frames_step * args.steps * ws / (ms / 1e3)
-    arcs_per_s = st0["arcs_expanded"] * args.steps * ws / (ms / 1e3)
+    (ms, e2e_s), (job_frames, job_arcs) = reduce_over_ranks(
+        dist, dev, [ms, e2e_s], [frames_step * args.steps, st0["arcs_expanded"] * args.steps])
+    value = job_rate(job_frames, ms / 1e3)
+    arcs_per_s = job_rate(job_arcs, ms / 1e3)
     kmean_s = float(np.mean(kern_ns)) / 1e9
     alg = algorithmic_bytes(st0, wl.V, esz)
     peak, peak_kind = load_peaks()
@@ -263,10 +310,11 @@ def run_gpu(args):
                    "l2": "inputs larger than L2 (320 MB log-probs, 218 MB graph); no flush"},
         "arcs_expanded_per_s": arcs_per_s,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                     "frac": achieved / peak, "traffic": measured_traffic(workload_name(wl), B),
+                     "peak_kind": peak_kind, "traffic_unit": "bytes per launch",
                      "kernel": "decode_kernel", "kernel_ms": kmean_s * 1e3,
                      "algorithmic_bytes": int(alg)},
-        "e2e": {"value": frames_step * args.steps * ws / e2e_s, "unit": "frames/s",
+        "e2e": {"value": job_rate(job_frames, e2e_s), "unit": "frames/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "phases_ms": {k[3:]: st0[k] / 1e6 for k in ("ns_init", "ns_max", "ns_expand", "ns_closure",
                                                      "ns_prune", "ns_prologue", "ns_commit", "ns_clear",

@@ -4,9 +4,9 @@
  *
  * The decoder follows the page "GPU WFST Beam-Search Decoder" (OASR
  * documentation, wfst_decoder_gpu).  Section numbers below are that page's.
- * It takes per-frame log-posteriors log_prob[B, T, V] and a decoding graph
- * (epsilon-free HLG style, or TLG style with epsilon arcs) and returns, per
- * utterance, the best word sequence and its score, optionally an
+ * Inputs: a batch of CTC log-posterior matrices log_prob[B, T, V] and a
+ * decoding graph (epsilon-free HLG style, or TLG style with epsilon arcs).
+ * Outputs, per utterance: the best word sequence and its score, optionally an
  * output_beam-pruned lattice, and, in streaming mode, a partial hypothesis
  * per chunk.
  *
@@ -16,8 +16,8 @@
  *   - Device pointers are CUDA device addresses on the decoder's device; host
  *     pointers are plain (pageable or pinned) host memory.  "stream" is a
  *     cudaStream_t passed as void* (NULL = the legacy default stream).
- *   - Calls on one decoder are serialised by an internal mutex (§10: an
- *     instance is thread-safe but serial); use one decoder per concurrent
+ *   - Calls on one decoder are serialised by an internal mutex (§10: one
+ *     instance runs one call at a time); use one decoder per concurrent
  *     caller.
  *   - A lane whose capacity was exceeded is not an error: its meta[2]
  *     overflow bits are set (§7 "Overflow bits") and its result may be
@@ -167,7 +167,8 @@ int wfst_decode(wfst_decoder* d, const void* log_probs, int32_t dtype, int64_t s
  * Lattice of one lane after wfst_decode or wfst_stream_finalize with
  * params.lattice = 1: every in-beam candidate (emitting, epsilon, final,
  * redirect) whose best complete path is within output_beam of the best path
- * (§3 "output_beam ... applied by the lattice backward prune only"; §7).
+ * (§3: output_beam acts only in this backward prune, never on the forward
+ * search; §7).
  * Records are sorted by (t, src_state, arc_id).  *n_records receives the
  * true count; at most `cap` records are written.  Errors: INVALID_ARG, STATE.
  */

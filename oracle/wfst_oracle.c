@@ -7,9 +7,10 @@
  * decoder that restates, one step at a time, the rules of the page
  * "GPU WFST Beam-Search Decoder" (OASR documentation, wfst_decoder_gpu):
  *
- *   §1 Purpose: one relaxation per frame over all out-arcs of the frontier,
- *      end = score[src] + arc_weight + log_prob[t][ilabel]; recombination by
- *      destination state keeping the best incoming arc; backtrack to words.
+ *   §1 Purpose: every frame relaxes each emitting arc leaving a frontier
+ *      token, with end = score[src] + arc_weight + log_prob[t][ilabel]; each
+ *      destination state keeps its best incoming candidate; the result is
+ *      backtracked to words.
  *   §3 Decoding Semantics: the dynamic-beam update (relax / widen / tighten,
  *      the last-frames min_active rule), admission end > exact_max - b with
  *      the exact per-step maximum, the final step, allow_partial, output_beam
