@@ -97,6 +97,8 @@ typedef struct {
 /* Turn off the per-token upper-bound skips of the max and expand passes
  * (§5.3 "Upper-bound skip"; exact either way — for identity tests). */
 #define WFST_OPT_NO_UB_SKIP 1
+/* Report capacity overflows without growing (see wfst_decode). */
+#define WFST_OPT_NO_GROW 4
 
 /* Per-lane capacities; 0 in any field selects its default. */
 typedef struct {
@@ -155,8 +157,15 @@ void wfst_decoder_free(wfst_decoder* d);
  * b*words_cap, forward order), word_lens [B] (TRUE length, may exceed
  * words_cap: re-issue with a larger buffer), scores [B] (fp32 path score
  * widened), meta [B*3] = {ok, reached_final, overflow bits}.
+ * Capacities grow on demand: lanes that overflow the winners log or lattice
+ * arena (bit 4), the frontier capacity (bit 16) or the best-path buffer (bit
+ * 32) have that capacity doubled (the workspace arrays are reallocated) and
+ * are decoded again, up to 12 times per call; a lane keeps its overflow bits
+ * only if the capacity is at its largest, memory runs out, or the decoder was
+ * created with WFST_OPT_NO_GROW.  Decoding is idempotent, so the re-run
+ * lanes give the results an unbounded decoder would give.
  * The call is stream-ordered on `stream` and returns after the results are
- * on the host.  Errors: INVALID_ARG, STATE, CUDA, TIMEOUT.
+ * on the host.  Errors: INVALID_ARG, STATE, CUDA, TIMEOUT, OOM.
  */
 int wfst_decode(wfst_decoder* d, const void* log_probs, int32_t dtype, int64_t stride_b,
                 int64_t stride_t, const int32_t* lens, int32_t B, int32_t T, void* stream,
@@ -229,6 +238,22 @@ int wfst_stream_release(wfst_decoder* d, int32_t channel);
 #define WFST_STAT_NS_PROLOGUE 15
 #define WFST_STAT_COUNT 23
 int wfst_stats(wfst_decoder* d, int64_t* out, int32_t n);
+
+/*
+ * Workspace of a decoder (host int64, n entries written, at most
+ * WFST_MEM_COUNT): device bytes held, then the current per-lane capacities
+ * (frontier tokens, winners-log entries, lattice records, best-path arcs) and
+ * the number of capacity doublings so far.  §6.2 of the page reports the
+ * decoder's memory the same way; here capacities only grow on demand.
+ */
+#define WFST_MEM_BYTES 0
+#define WFST_MEM_FRONTIER_CAP 1
+#define WFST_MEM_LOG_CAP 2
+#define WFST_MEM_LATTICE_CAP 3
+#define WFST_MEM_PATH_CAP 4
+#define WFST_MEM_GROWS 5
+#define WFST_MEM_COUNT 6
+int wfst_mem_stats(wfst_decoder* d, int64_t* out, int32_t n);
 
 /*
  * Offline decode that allocates nothing (no device or pinned memory, no

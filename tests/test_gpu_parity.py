@@ -240,7 +240,7 @@ def test_capacity_overflow_is_flagged_and_recovers(W, graphs):
     lens = np.full(2, 50, np.int32)
     p = wl_params(wl)
     caps = W.Capacity(64, 0, 0, 0)      # frontier of at most 64 tokens per frame
-    G, D = gpu_decoder(W, g, p, 2, 50, caps=caps)
+    G, D = gpu_decoder(W, g, p, 2, 50, caps=caps, options=W.OPT_NO_GROW)
     out = D.decode(_cuda(lp), lens)
     assert all(o["overflow"] & W.OVF_KEPT for o in out)
     # a full-capacity decoder on the same graph is unaffected, and a small
@@ -253,7 +253,7 @@ def test_capacity_overflow_is_flagged_and_recovers(W, graphs):
         if out2[b]["overflow"] == 0:
             assert_lane_equal(out2[b], ref, f"after overflow lane {b}")
     caps = W.Capacity(0, 1000, 0, 0)    # winners log too small
-    G2, D2 = gpu_decoder(W, g, p, 2, 50, caps=caps, graph=G)
+    G2, D2 = gpu_decoder(W, g, p, 2, 50, caps=caps, graph=G, options=W.OPT_NO_GROW)
     out3 = D2.decode(_cuda(lp), lens)
     assert all(o["overflow"] & W.OVF_ARENA for o in out3)
 
@@ -277,3 +277,34 @@ def test_upper_bound_skip_is_exact(W, graphs):
         assert list(o1[b]["words"]) == list(o0[b]["words"]) and o1[b]["score"] == o0[b]["score"]
     for k in ("arcs_expanded", "sum_n", "sum_D", "sum_a", "sum_m"):
         assert s1[k] == s0[k], k
+
+
+def test_capacities_grow_until_results_are_exact(W, graphs):
+    """Undersized frontier, winners-log, lattice and path capacities grow on
+    demand: every lane ends without overflow bits and equals the oracle,
+    lattice included; the memory report shows the doublings."""
+    for wi, caps in ((1, (64, 1000, 0, 8)), (0, (16, 256, 64, 4))):
+        wl = synth.workload(wi)
+        g = graphs(wi)
+        T = 40
+        lanes = list(range(3))
+        lp = synth.make_log_probs(wi, lanes=lanes, T=T)
+        lens = np.array([T, T - 5, 7], np.int32)
+        p = wl_params(wl, lattice=(wi == 0))
+        G, D = gpu_decoder(W, g, p, len(lanes), T, caps=W.Capacity(*caps))
+        m0 = D.mem_stats()
+        out = D.decode(_cuda(lp), lens)
+        m1 = D.mem_stats()
+        OG = oracle.Graph(g)
+        for b in range(len(lanes)):
+            ref = oracle_lane(OG, lp[b], lens[b], p)
+            assert_lane_equal(out[b], ref, f"workload {wi} lane {b}")
+            if p["lattice"] and ref["ok"]:
+                assert_lattice_equal(D.lattice(b), ref["lattice"], f"workload {wi} lane {b}")
+        assert m1["grows"] > m0["grows"]
+        assert m1["frontier_cap"] > m0["frontier_cap"] and m1["log_cap"] > m0["log_cap"]
+        # a second call on the grown decoder needs no further growth
+        D.decode(_cuda(lp), lens)
+        assert D.mem_stats()["grows"] == m1["grows"]
+        D.close()
+        G.close()

@@ -36,7 +36,7 @@ LAT_DTYPE = np.dtype([("t", "<i4"), ("src_state", "<i4"), ("dst_state", "<i4"),
 EXPORTED = ["wfst_graph_upload", "wfst_graph_info", "wfst_graph_free", "wfst_decoder_create",
             "wfst_decoder_free", "wfst_decode", "wfst_lattice_export", "wfst_stream_create",
             "wfst_stream_advance", "wfst_stream_finalize", "wfst_stream_release", "wfst_stats",
-            "wfst_decode_static", "wfst_last_error"]
+            "wfst_decode_static", "wfst_mem_stats", "wfst_last_error"]
 
 
 class WfstError(RuntimeError):
@@ -104,6 +104,7 @@ def load(build_if_missing: bool = False):
         L.wfst_stream_finalize.argtypes = [P, P, i32, P, P, i32, P, P, P]
         L.wfst_stream_release.argtypes = [P, i32]
         L.wfst_stats.argtypes = [P, P, i32]
+        L.wfst_mem_stats.argtypes = [P, P, i32]
         for name in EXPORTED:
             if name not in ("wfst_last_error", "wfst_graph_free", "wfst_decoder_free"):
                 getattr(L, name).restype = C.c_int
@@ -222,6 +223,12 @@ def wfst_stats(h):
     return dict(zip(STAT_NAMES, out.tolist()))
 
 
+def wfst_mem_stats(h):
+    out = np.zeros(len(MEM_NAMES), np.int64)
+    _check(load().wfst_mem_stats(h, _ptr(out), len(MEM_NAMES)))
+    return dict(zip(MEM_NAMES, out.tolist()))
+
+
 # ------------------------------------------------------------ convenience wrappers
 
 class Graph:
@@ -259,6 +266,8 @@ class Graph:
 
 
 OPT_NO_UB_SKIP = 1
+OPT_NO_GROW = 4
+MEM_NAMES = ["bytes", "frontier_cap", "log_cap", "lattice_cap", "path_cap", "grows"]
 
 
 def make_params(search_beam=20.0, output_beam=8.0, min_active=30, max_active=10000,
@@ -329,6 +338,9 @@ class Decoder:
 
     def stats(self):
         return wfst_stats(self.h)
+
+    def mem_stats(self):
+        return wfst_mem_stats(self.h)
 
     # streaming
     def stream_create(self) -> int:

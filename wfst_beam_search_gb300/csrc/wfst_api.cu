@@ -271,7 +271,9 @@ struct wfst_decoder {
   DevWork w{};
   int grid[2] = {0, 0};
   std::vector<void*> allocs;
+  std::vector<size_t> alloc_bytes;
   int64_t bytes = 0;
+  int64_t grows = 0;              // capacity doublings so far
   // pinned host mirrors
   LaneCall* h_calls = nullptr;
   Result* h_res = nullptr;
@@ -299,9 +301,25 @@ static cudaError_t dalloc(wfst_decoder* d, T** p, size_t n, bool zero = false) {
   cudaError_t e = cudaMalloc((void**)p, b);
   if (e != cudaSuccess) return e;
   d->allocs.push_back(*p);
+  d->alloc_bytes.push_back(b);
   d->bytes += (int64_t)b;
   if (zero) e = cudaMemset(*p, 0, b);
   return e;
+}
+
+// Replace one workspace array by a fresh one of n elements (contents lost).
+template <typename T>
+static cudaError_t dregrow(wfst_decoder* d, T** p, size_t n) {
+  for (size_t i = 0; i < d->allocs.size(); i++) {
+    if (d->allocs[i] != (void*)*p) continue;
+    cudaFree(*p);
+    d->bytes -= (int64_t)d->alloc_bytes[i];
+    d->allocs.erase(d->allocs.begin() + (long)i);
+    d->alloc_bytes.erase(d->alloc_bytes.begin() + (long)i);
+    break;
+  }
+  *p = nullptr;
+  return dalloc(d, p, n, false);
 }
 
 static void decoder_destroy(wfst_decoder* d) {
@@ -605,6 +623,54 @@ static void write_lane(wfst_decoder* d, int32_t lane, int32_t out_index, int32_t
   }
 }
 
+// Offline capacity growth: double the capacity behind each overflow seen
+// (winners log, lattice arena, frontier up to num_states, best path) and
+// reallocate those arrays.  WFST_ERR_CAPACITY when nothing can grow.
+static int grow_capacities(wfst_decoder* d, bool g_log, bool g_lat, bool g_q, bool g_path) {
+  DevWork& w = d->w;
+  const size_t L = (size_t)d->L;
+  const DevGraph& G = d->g->dg;
+  bool any = false;
+  cudaError_t e = cudaSuccess;
+  if (g_log && w.log_cap < (int64_t)INT32_MAX - 1) {
+    w.log_cap = std::min<int64_t>(2 * w.log_cap, (int64_t)INT32_MAX - 1);
+    e = dregrow(d, &w.wlog, L * (size_t)w.log_cap);
+    if (e == cudaSuccess && w.lattice) e = dregrow(d, &w.bwd, L * (size_t)w.log_cap);
+    any = true;
+  }
+  if (e == cudaSuccess && g_lat && w.lattice && w.lat_cap < ((int64_t)1 << 40)) {
+    w.lat_cap *= 2;
+    e = dregrow(d, &w.lat, L * (size_t)w.lat_cap);
+    if (e == cudaSuccess) e = dregrow(d, &w.lat_out, L * (size_t)w.lat_cap);
+    any = true;
+  }
+  if (e == cudaSuccess && g_q && w.qcap < (int64_t)G.N) {
+    w.qcap = std::min<int64_t>(2 * w.qcap, (int64_t)G.N);
+    e = dregrow(d, &w.front, 2 * L * (size_t)w.qcap);
+    if (e == cudaSuccess) e = dregrow(d, &w.score, 2 * L * (size_t)w.qcap);
+    if (e == cudaSuccess && G.has_eps) e = dregrow(d, &w.wl, 2 * L * (size_t)w.qcap);
+    any = true;
+  }
+  if (e == cudaSuccess && g_path && w.path_cap < (int64_t)INT32_MAX / 2) {
+    w.path_cap = std::min<int64_t>(2 * w.path_cap, (int64_t)INT32_MAX / 2);
+    e = dregrow(d, &w.path, L * (size_t)w.path_cap);
+    any = true;
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e == cudaErrorMemoryAllocation ? fail(WFST_ERR_OOM, "decode: out of device memory while growing capacities")
+                                          : cuda_fail(e, "decode: capacity growth");
+  }
+  if (!any) return fail(WFST_ERR_CAPACITY, "decode: capacities are at their largest");
+  d->grows++;
+  return WFST_OK;
+}
+
+static void stats_add(int64_t* acc, const int64_t* s) {
+  for (int i = 0; i < WFST_STAT_COUNT; i++)
+    acc[i] = (i == WFST_STAT_STEPS) ? std::max(acc[i], s[i]) : acc[i] + s[i];
+}
+
 extern "C" int wfst_decode(wfst_decoder* d, const void* log_probs, int32_t dtype, int64_t stride_b,
                            int64_t stride_t, const int32_t* lens, int32_t B, int32_t T, void* stream,
                            int32_t* words, int32_t words_cap, int32_t* word_lens, double* scores,
@@ -649,15 +715,64 @@ extern "C" int wfst_decode(wfst_decoder* d, const void* log_probs, int32_t dtype
   }
   rc = run_call(d, lp, dtype, stride_b, stride_t, st, words_cap);
   if (rc != WFST_OK) return rc;
-  for (int32_t b = 0; b < B; b++) {
-    write_lane(d, b, b, words, words_cap, word_lens, scores, meta);
-    const int ovf = d->h_lanes[b].overflow;
-    d->lat_valid[b] = d->p.lattice && d->h_res[b].ok && !(ovf & (kOvfArena | kOvfKept));
-    if (ovf & kOvfKept) {
-      rc = sanitize(d, b, st);
-      if (rc != WFST_OK) return rc;
+  int64_t acc[WFST_STAT_COUNT];
+  std::memcpy(acc, d->stats, sizeof(acc));
+  std::vector<int32_t> ran(B);
+  for (int32_t b = 0; b < B; b++) ran[b] = b;
+  for (int round = 0;; round++) {
+    std::vector<int32_t> over;
+    for (int32_t b : ran) {
+      write_lane(d, b, b, words, words_cap, word_lens, scores, meta);
+      const int ovf = d->h_lanes[b].overflow;
+      d->lat_valid[b] = d->p.lattice && d->h_res[b].ok && !(ovf & (kOvfArena | kOvfKept));
+      if (ovf & kOvfKept) {
+        rc = sanitize(d, b, st);
+        if (rc != WFST_OK) return rc;
+      }
+      if (ovf & (kOvfArena | kOvfKept | kOvfPath)) over.push_back(b);
     }
+    if (over.empty() || (d->p.options & WFST_OPT_NO_GROW) || round >= kMaxGrowRounds) break;
+    bool g_log = false, g_lat = false, g_q = false, g_path = false;
+    std::vector<unsigned long long> lat_n;
+    if (d->p.lattice) {
+      lat_n.resize(d->L);
+      CU(cudaMemcpyAsync(lat_n.data(), d->w.lat_cnt, sizeof(unsigned long long) * d->L, cudaMemcpyDeviceToHost, st),
+         "lattice counts D2H");
+      CU(cudaStreamSynchronize(st), "lattice counts D2H");
+    }
+    for (int32_t b : over) {
+      const int ovf = d->h_lanes[b].overflow;
+      if (ovf & kOvfKept) g_q = true;
+      if (ovf & kOvfPath) g_path = true;
+      if (ovf & kOvfArena) {
+        const bool lat_full = d->p.lattice && lat_n[b] > (unsigned long long)d->w.lat_cap;
+        if (lat_full) g_lat = true;
+        if (d->h_lanes[b].cursor > d->w.log_cap || !lat_full) g_log = true;
+      }
+    }
+    rc = grow_capacities(d, g_log, g_lat, g_q, g_path);
+    if (rc == WFST_ERR_CAPACITY) break;  // already at the largest sizes: the bits stay set
+    if (rc != WFST_OK) return rc;
+    // a regrown lattice arena has lost every lane's records: all lanes run again
+    if (g_lat && d->p.lattice) {
+      ran.resize(B);
+      for (int32_t b = 0; b < B; b++) ran[b] = b;
+    } else {
+      ran = over;
+    }
+    for (int32_t l = 0; l < d->L; l++) d->h_calls[l].row = -1;
+    for (int32_t b : ran) {
+      LaneCall& c = d->h_calls[b];
+      c.row = b;
+      c.nframes = lens[b];
+      c.flags = kCallInit | kCallFinal;
+      c.t_eff = lens[b];
+    }
+    rc = run_call(d, lp, dtype, stride_b, stride_t, st, words_cap);
+    if (rc != WFST_OK) return rc;
+    stats_add(acc, d->stats);
   }
+  std::memcpy(d->stats, acc, sizeof(acc));
   CU(cudaStreamSynchronize(st), "decode");
   return WFST_OK;
 }
@@ -836,6 +951,14 @@ extern "C" int wfst_stream_release(wfst_decoder* d, int32_t channel) {
   d->chan_state[channel] = 0;
   d->chan_t[channel] = 0;
   d->lat_valid[channel] = 0;
+  return WFST_OK;
+}
+
+extern "C" int wfst_mem_stats(wfst_decoder* d, int64_t* out, int32_t n) {
+  if (!d || !out || n < 0) return fail(WFST_ERR_INVALID_ARG, "mem_stats: bad argument");
+  std::lock_guard<std::mutex> lock(d->mu);
+  const int64_t v[WFST_MEM_COUNT] = {d->bytes, d->w.qcap, d->w.log_cap, d->w.lat_cap, d->w.path_cap, d->grows};
+  for (int32_t i = 0; i < n && i < WFST_MEM_COUNT; i++) out[i] = v[i];
   return WFST_OK;
 }
 

@@ -15,6 +15,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kOvfArena = 4;
 constexpr int kOvfKept = 16;
 constexpr int kOvfPath = 32;
+constexpr int kMaxGrowRounds = 12;  // offline capacity doublings per decode call
 
 // lattice record flags
 constexpr int kRecEps = 1;
