@@ -33,7 +33,7 @@ namespace wfst {
 
 constexpr unsigned long long kTimeoutNs = 4000000000ull;  // 4 s per barrier wait
 constexpr int kSPT = kTile / 32;                           // slots per lane per tile
-constexpr int kCB = 4;                                     // tokens per thread per commit batch
+constexpr int kCB = 5;                                     // tokens per thread per commit batch
 
 enum Phase { kNone = 0, kEmit = 1, kFin = 2, kPart = 3 };
 
@@ -1081,7 +1081,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
       const int total = S.pre_b[L];
       const int wlane = tid & 31;
       // warp-uniform trip count: the seed below is a warp-collective
-      for (int wb = blockIdx.x * kThreads * kCB + (tid & ~31); wb < total; wb += G * kThreads * kCB) {
+      // every CTA takes an equal contiguous share (one batch per thread when
+      // the frame fits G * kThreads * kCB tokens)
+      const int per = (total + G - 1) / G;
+      const int c0 = min(total, blockIdx.x * per), c1 = min(total, c0 + per);
+      for (int wb = c0 + (tid & ~31); wb < c1; wb += kThreads * kCB) {
         const int g0 = wb + wlane;
         unsigned seed = 0;  // bit k: token k of this thread seeds the max
         int lk[kCB];
@@ -1091,7 +1095,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
 #pragma unroll
         for (int k = 0; k < kCB; k++) {
           const int gi = g0 + k * kThreads;
-          v[k] = gi < total;
+          v[k] = gi < c1;
           lk[k] = v[k] ? find_lane(S.pre_b, L, gi) : 0;
           pk[k] = v[k] ? gi - S.pre_b[lk[k]] : 0;
           st[k] = v[k] ? __ldcg(&w.front[ql(w, S.lane[lk[k]].t & 1, lk[k]) + pk[k]].state) : 0;
@@ -1163,14 +1167,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     prof_mark(prof, tsub, kProfCommit);
     {  // clear frame t-1's recombination entries
       const int total = S.pre_c[L];
-      for (int g0 = blockIdx.x * kThreads * kCB + tid; g0 < total; g0 += G * kThreads * kCB) {
+      const int per = (total + G - 1) / G;
+      const int c0 = min(total, blockIdx.x * per), c1 = min(total, c0 + per);
+      for (int g0 = c0 + tid; g0 < c1; g0 += kThreads * kCB) {
         int32_t st[kCB];
         int lk[kCB];
         bool v[kCB];
 #pragma unroll
         for (int k = 0; k < kCB; k++) {
           const int gi = g0 + k * kThreads;
-          v[k] = gi < total;
+          v[k] = gi < c1;
           lk[k] = v[k] ? find_lane(S.pre_c, L, gi) : 0;
           st[k] = v[k] ? __ldcg(&w.front[ql(w, (S.lane[lk[k]].t - 1) & 1, lk[k]) + gi - S.pre_c[lk[k]]].state)
                        : 0;
