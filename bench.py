@@ -227,7 +227,8 @@ def run_gpu(args):
     wl = synth.workload(args.workload)
     g = synth.make_graph(args.workload)
     G = W.Graph(g, device=local)
-    params = W.make_params(wl.search_beam, wl.output_beam, wl.min_active, wl.max_active, True, False,
+    params = W.make_params(wl.search_beam, wl.output_beam, wl.min_active, wl.max_active, True,
+                           wl.lattice and wl.streaming, streaming=wl.streaming,
                            options=W.OPT_NO_UB_SKIP if args.no_ub_skip else 0)
     nl = args.lanes or wl.B
     caps = W.Capacity(args.frontier_cap, args.log_cap, 0, 0) if (args.log_cap or args.frontier_cap) else None
@@ -248,13 +249,43 @@ def run_gpu(args):
     sc = np.zeros(B, np.float64)
     meta = np.zeros((B, 3), np.int32)
 
-    def step(src_ptr):
-        W.wfst_decode(D.h, src_ptr, dt, sb, st, W._ptr(lens_np), B, T, W._stream(stream),
+    def step_offline(src):
+        p_, dt_, sb_, st_, _, _ = W._lp_args(src)
+        W.wfst_decode(D.h, p_, dt_, sb_, st_, W._ptr(lens_np), B, T, W._stream(stream),
                       W._ptr(words), words_cap, W._ptr(wl_), W._ptr(sc), W._ptr(meta))
         return W.wfst_stats(D.h)
 
+    def step_stream(src):
+        """One streaming pass: open a channel per lane, feed every chunk with a
+        partial hypothesis per chunk, finalize (final step + lattice prune),
+        release.  Counters are summed over the calls."""
+        chans = np.ascontiguousarray([D.stream_create() for _ in range(B)], np.int32)
+        tot = None
+        for s0 in range(0, T, wl.chunk):
+            cl = np.ascontiguousarray(np.clip(lens_np - s0, 0, wl.chunk), np.int32)
+            view = src[:, s0:s0 + wl.chunk]
+            p_, dt_, sb_, st_, _, ct = W._lp_args(view)
+            W.wfst_stream_advance(D.h, W._ptr(chans), B, p_, dt_, sb_, st_, W._ptr(cl), ct, 1,
+                                  W._stream(stream), W._ptr(words), words_cap, W._ptr(wl_), W._ptr(sc),
+                                  W._ptr(meta))
+            s_ = W.wfst_stats(D.h)
+            tot = s_ if tot is None else {k: (max(tot[k], v) if k == "steps" else tot[k] + v) for k, v in s_.items()}
+        W.wfst_stream_finalize(D.h, W._ptr(chans), B, W._stream(stream), W._ptr(words), words_cap,
+                               W._ptr(wl_), W._ptr(sc), W._ptr(meta))
+        s_ = W.wfst_stats(D.h)
+        tot = {k: (max(tot[k], v) if k == "steps" else tot[k] + v) for k, v in s_.items()}
+        for c in chans:
+            W.wfst_stream_release(D.h, int(c))
+        return tot
+
+    calls_per_step = (-(-T // wl.chunk) + 1) if wl.streaming else 1
+
+    def step(src_is_host):
+        src = lp_pin if src_is_host else lp_dev
+        return step_stream(src) if wl.streaming else step_offline(src)
+
     for _ in range(args.warmup):
-        step(ptr)
+        step(False)
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -265,7 +296,7 @@ def run_gpu(args):
     kern_ns, stats = [], []
     ev0.record(stream)
     for _ in range(args.steps):
-        s = step(ptr)
+        s = step(False)
         kern_ns.append(s["kernel_ns"])
         stats.append(s)
     ev1.record(stream)
@@ -274,11 +305,10 @@ def run_gpu(args):
         dist.barrier()
     ms = ev0.elapsed_time(ev1)
     # end to end through the C ABI with pinned host buffers (H2D inside the call)
-    pin_ptr = W._ptr(lp_pin)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        step(pin_ptr)
+        step(True)
     e2e_s = time.perf_counter() - t0
     clk = clocks.stop()
     frames_step = int(lens.sum())
@@ -308,7 +338,9 @@ def run_gpu(args):
                    "global_batch": B * ws, "frames_per_utt": T, "vocab": wl.V, "log_probs": wl.dtype,
                    "search_beam": wl.search_beam, "max_active": wl.max_active,
                    "min_active": wl.min_active, "parallelism": f"replicas x{ws} (lanes sharded)",
-                   "l2": "inputs larger than L2 (320 MB log-probs, 218 MB graph); no flush"},
+                   "l2": "inputs larger than L2 (320 MB log-probs, 218 MB graph); no flush",
+                   "mode": (f"streaming: {wl.chunk}-frame chunks, partial per chunk, finalize with lattice"
+                            if wl.streaming else "offline")},
         "arcs_expanded_per_s": arcs_per_s,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": measured_traffic(workload_name(wl), B),
@@ -322,7 +354,7 @@ def run_gpu(args):
                                                      "ns_max_tiles", "ns_wait_x", "ns_expand_tiles",
                                                      "ns_final", "ns_wait_y")},
         "steps_per_decode": st0["steps"], "barriers_per_decode": st0["barriers"],
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * calls_per_step,
         "lanes_ok": res_ok,
         "clocks": clk,
         "cpu_baseline": cpu,

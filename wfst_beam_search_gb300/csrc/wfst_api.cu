@@ -940,8 +940,12 @@ extern "C" int wfst_stream_release(wfst_decoder* d, int32_t channel) {
   if (channel < 0 || channel >= d->L || d->chan_state[channel] == 0)
     return fail(WFST_ERR_INVALID_ARG, "stream_release: channel is not in use");
   DeviceGuard dgd(d->g->device);
-  int rc = sanitize(d, channel, (cudaStream_t)0);
-  if (rc != WFST_OK) return rc;
+  // a finalized channel's entries were cleared by its final step, unless
+  // tokens were dropped past the frontier capacity
+  if (d->chan_state[channel] != 2 || (d->h_lanes[channel].overflow & kOvfKept)) {
+    int rc = sanitize(d, channel, (cudaStream_t)0);
+    if (rc != WFST_OK) return rc;
+  }
   LaneState s;
   std::memset(&s, 0, sizeof(s));
   CU(cudaMemcpy(&s.eps_pass, &d->w.lanes[channel].eps_pass, sizeof(uint32_t), cudaMemcpyDeviceToHost), "release");
