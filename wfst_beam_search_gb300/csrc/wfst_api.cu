@@ -20,8 +20,8 @@
 
 namespace wfst {
 cudaError_t launch_decode(const RunArgs& a, int dtype, int grid, cudaStream_t st);
-cudaError_t max_grid(int dtype, int* grid);
-size_t smem_bytes();
+cudaError_t max_grid(int dtype, int L, int* grid);
+size_t smem_bytes(int L);
 }  // namespace wfst
 
 using namespace wfst;
@@ -438,8 +438,8 @@ extern "C" int wfst_decoder_create(wfst_graph* g, const wfst_params* params, int
     }
     e = cudaMemcpy(w.lanes, init.data(), sizeof(LaneState) * L, cudaMemcpyHostToDevice);
   }
-  if (e == cudaSuccess) e = max_grid(0, &d->grid[0]);
-  if (e == cudaSuccess) e = max_grid(1, &d->grid[1]);
+  if (e == cudaSuccess) e = max_grid(0, max_lanes, &d->grid[0]);
+  if (e == cudaSuccess) e = max_grid(1, max_lanes, &d->grid[1]);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     decoder_destroy(d);

@@ -62,13 +62,18 @@ struct WStage {                   // one warp's staged tokens of its current til
   int32_t tpos[kTokCap];          // epsilon worklists: the token's position in its frame
 };
 
+// Shared memory of a CTA: this struct, then the per-lane arrays it points to,
+// sized by the launch's lane count (shared memory left unused is L1 cache on
+// this part, and the log-prob gathers live on L1 hits).
 struct Smem {
-  SmLane lane[kMaxLanes];
-  int32_t pre_a[kMaxLanes + 1];   // work units per lane, exclusive prefix (tiles)
-  int32_t pre_b[kMaxLanes + 1];   // commit tokens / tasks
-  int32_t pre_c[kMaxLanes + 1];   // clear tokens
-  int32_t pre_d[kMaxLanes + 1];   // lattice records to resolve
-  WStage ws[kWarps];
+  SmLane* lane;                   // [L] lane mirrors
+  int32_t* pre_a;                 // [L+1] work units per lane, exclusive prefix (tiles)
+  int32_t* pre_b;                 // [L+1] commit tokens / tasks
+  int32_t* pre_c;                 // [L+1] clear tokens
+  int32_t* pre_d;                 // [L+1] lattice records to resolve
+  int32_t* pre_e;                 // [L+1] lattice prune: records of the current group
+  int64_t* glo;                   // [L] lattice prune: first record of the current group
+  alignas(16) WStage ws[kWarps];
   float redf[kWarps];
   uint32_t redu[kWarps];
   int32_t scan_tmp[kWarps];
@@ -823,34 +828,43 @@ __device__ bool lattice_prune(const RunArgs& a, Smem& S, unsigned& epoch) {
     for (int pass = 0; pass < npass; pass++, pass_no++) {
       const int fl = pass_no % 3;
       if (blockIdx.x == 0 && tid == 0) w.bar->changed[(pass_no + 1) % 3] = 0u;
-      for (int l = 0; l < L; l++) {
+      // this group's record range of every lane, flattened into one index
+      // space so that all lanes' records are spread over the whole grid
+      for (int l = tid; l < L; l += kThreads) {
         const SmLane& s = S.lane[l];
-        if (!s.closure) continue;
-        const int T = s.t;
-        const int64_t* B = w.lat_groups + (size_t)l * (w.max_frames + 2);
-        const int64_t total = (int64_t)min(__ldcg(&w.lat_cnt[l]), (unsigned long long)w.lat_cap);
-        int64_t lo, hi;
-        if (j == 0) {
-          lo = B[T];
-          hi = total;
-        } else {
-          const int r = T - 1 - (j - 1) / 2;  // R_r, r >= -1
-          if (r < -1) continue;
-          lo = (r < 0) ? 0 : B[r];
-          hi = B[r + 1];
+        int64_t lo = 0, hi = 0;
+        if (s.closure) {
+          const int T = s.t;
+          const int64_t* B = w.lat_groups + (size_t)l * (w.max_frames + 2);
+          if (j == 0) {
+            lo = B[T];
+            hi = (int64_t)min(__ldcg(&w.lat_cnt[l]), (unsigned long long)w.lat_cap);
+          } else {
+            const int r = T - 1 - (j - 1) / 2;  // R_r, r >= -1
+            if (r >= -1) {
+              lo = (r < 0) ? 0 : B[r];
+              hi = B[r + 1];
+            }
+          }
         }
-        const LatRec* R = w.lat + (size_t)l * w.lat_cap;
+        S.glo[l] = lo;
+        S.pre_e[l] = (int32_t)max((int64_t)0, hi - lo);
+      }
+      __syncthreads();
+      lane_scan(S.pre_e, L);
+      const int gtotal = S.pre_e[L];
+      for (int gi = (int)gstart; gi < gtotal; gi += (int)gstride) {
+        const int l = find_lane(S.pre_e, L, gi);
+        const int64_t r = S.glo[l] + (gi - S.pre_e[l]);
+        const LatRec rec = w.lat[(size_t)l * w.lat_cap + r];
+        const int flags = rec.frame_flags & 15;
+        if (flags & kRecDead) continue;
+        if (j > 0 && (((flags & kRecEps) != 0) != eps_group)) continue;
         uint32_t* bw = w.bwd + (size_t)l * w.log_cap;
-        for (int64_t r = lo + gstart; r < hi; r += gstride) {
-          const LatRec rec = R[r];
-          const int flags = rec.frame_flags & 15;
-          if (flags & kRecDead) continue;
-          if (j > 0 && (((flags & kRecEps) != 0) != eps_group)) continue;
-          const float bd = rec.dst_tok < 0 ? 0.0f : unord_f(__ldcg(bw + rec.dst_tok));
-          const unsigned ov = ord_f(__fadd_rn(rec.arcscore, bd));
-          const unsigned old = atomicMax(bw + rec.src_tok, ov);
-          if (eps_group && ov > old) w.bar->changed[fl] = 1u;
-        }
+        const float bd = rec.dst_tok < 0 ? 0.0f : unord_f(__ldcg(bw + rec.dst_tok));
+        const unsigned ov = ord_f(__fadd_rn(rec.arcscore, bd));
+        const unsigned old = atomicMax(bw + rec.src_tok, ov);
+        if (eps_group && ov > old) w.bar->changed[fl] = 1u;
       }
       if (!grid_sync(a, S, epoch)) return false;
       if (eps_group && ld_acquire(&w.bar->changed[fl]) == 0u) break;
@@ -891,10 +905,35 @@ __device__ bool lattice_prune(const RunArgs& a, Smem& S, unsigned& epoch) {
 
 // ------------------------------------------------------------------ the kernel
 
+// Dynamic shared memory of a launch over L lanes, and the carving of it.
+__host__ __device__ inline size_t smem_lane_offset() { return (sizeof(Smem) + 15) & ~(size_t)15; }
+__host__ __device__ inline size_t smem_size(int L) {
+  size_t o = smem_lane_offset() + (size_t)L * sizeof(SmLane);
+  o += 5 * (size_t)(L + 1) * sizeof(int32_t);
+  o = (o + 7) & ~(size_t)7;
+  return o + (size_t)L * sizeof(int64_t);
+}
+__device__ inline void smem_carve(Smem& S, unsigned char* raw, int L) {
+  unsigned char* p = raw + smem_lane_offset();
+  S.lane = reinterpret_cast<SmLane*>(p);
+  p += (size_t)L * sizeof(SmLane);
+  int32_t* q = reinterpret_cast<int32_t*>(p);
+  S.pre_a = q; q += L + 1;
+  S.pre_b = q; q += L + 1;
+  S.pre_c = q; q += L + 1;
+  S.pre_d = q; q += L + 1;
+  S.pre_e = q; q += L + 1;
+  p = reinterpret_cast<unsigned char*>(q);
+  p = reinterpret_cast<unsigned char*>(((size_t)p + 7) & ~(size_t)7);
+  S.glo = reinterpret_cast<int64_t*>(p);
+}
+
 template <typename LP>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
+  if (threadIdx.x == 0) smem_carve(S, smem_raw, a.nlanes);
+  __syncthreads();
   const DevWork& w = a.w;
   const DevGraph& g = a.g;
   const int L = a.nlanes;
@@ -1498,17 +1537,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
 
 // ------------------------------------------------------------------ launcher
 
-size_t smem_bytes() { return sizeof(Smem); }
+size_t smem_bytes(int L) { return smem_size(L); }
 
 template <typename LP>
 static cudaError_t prepare_t() {
   return cudaFuncSetAttribute(decode_kernel<LP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)sizeof(Smem));
+                              (int)smem_size(kMaxLanes));
 }
 
 cudaError_t launch_decode(const RunArgs& a, int dtype, int grid, cudaStream_t st) {
   void* args[] = {(void*)&a};
-  const size_t sm = sizeof(Smem);
+  const size_t sm = smem_size(a.nlanes);
   if (dtype == 1) {
     cudaError_t e = prepare_t<__half>();
     if (e != cudaSuccess) return e;
@@ -1521,13 +1560,14 @@ cudaError_t launch_decode(const RunArgs& a, int dtype, int grid, cudaStream_t st
                                      st);
 }
 
-cudaError_t max_grid(int dtype, int* grid) {
+// Cooperative grid for a launch over L lanes: resident CTAs per SM x SMs.
+cudaError_t max_grid(int dtype, int L, int* grid) {
   int dev = 0, sms = 0, per = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const size_t sm = sizeof(Smem);
+  const size_t sm = smem_size(L);
   if (dtype == 1) {
     e = prepare_t<__half>();
     if (e == cudaSuccess)

@@ -44,7 +44,7 @@
 
 namespace wfst {
 cudaError_t launch_decode(const RunArgs& a, int dtype, int grid, cudaStream_t st);
-cudaError_t max_grid(int dtype, int* grid);
+cudaError_t max_grid(int dtype, int L, int* grid);
 int api_fail(int code, const char* msg);
 int api_cuda_fail(cudaError_t e, const char* what);
 const DevGraph* api_graph(const wfst_graph* g, int* device);
@@ -164,8 +164,8 @@ int setup_device(DeviceSlot& s) {
   cudaError_t e = cudaGetSymbolAddress(&ptr, g_scratch);
   if (e != cudaSuccess) return api_cuda_fail(e, "decode_static: cudaGetSymbolAddress of the scratch region");
   if (!ptr) return api_fail(WFST_ERR_CUDA, "decode_static: the scratch region has no device address");
-  e = max_grid(0, &s.grid[0]);
-  if (e == cudaSuccess) e = max_grid(1, &s.grid[1]);
+  e = max_grid(0, kStaticLanes, &s.grid[0]);
+  if (e == cudaSuccess) e = max_grid(1, kStaticLanes, &s.grid[1]);
   if (e != cudaSuccess) return api_cuda_fail(e, "decode_static: occupancy query");
   if (s.grid[0] < 1 || s.grid[1] < 1)
     return api_fail(WFST_ERR_CUDA, "decode_static: the decode kernel cannot be made resident");
