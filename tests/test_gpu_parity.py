@@ -308,3 +308,90 @@ def test_capacities_grow_until_results_are_exact(W, graphs):
         assert D.mem_stats()["grows"] == m1["grows"]
         D.close()
         G.close()
+
+
+# ------------------------------------------------------------ maximum sizes, degenerate graphs
+
+def test_max_lanes_256(W):
+    """The largest decoder (256 lanes, every lane a different utterance) on
+    a small random graph equals the oracle lane by lane."""
+    rng = np.random.default_rng(5150)
+    g = synth.random_tiny_graph(rng, 30, 6, max_deg=4, p_eps=0.2, dyadic=False, p_final=0.3)
+    B, T = 256, 12
+    lp = np.log(rng.dirichlet(np.ones(6), size=(B, T))).astype(np.float32)
+    lens = rng.integers(0, T + 1, size=B).astype(np.int32)
+    p = dict(search_beam=6.0, output_beam=2.0, min_active=2, max_active=8, allow_partial=True, lattice=True)
+    G, D = gpu_decoder(W, g, p, B, T)
+    out = D.decode(_cuda(lp), lens)
+    OG = oracle.Graph(g)
+    for b in range(B):
+        ref = oracle_lane(OG, lp[b], lens[b], p)
+        assert_lane_equal(out[b], ref, f"lane {b}")
+        if ref["ok"] and b % 16 == 0:
+            assert_lattice_equal(D.lattice(b), ref["lattice"], f"lane {b}")
+
+
+def test_vocab_at_the_label_limit(W):
+    """V = 65534, the largest vocabulary the 16-bit label column holds, with
+    arcs on the highest labels."""
+    rng = np.random.default_rng(65534)
+    V, N = 65534, 12
+    src = np.repeat(np.arange(N), 3)
+    dst = rng.integers(0, N, size=src.size)
+    il = rng.integers(V - 40, V, size=src.size)
+    il[::3] = 0
+    ol = np.where(rng.random(src.size) < 0.5, rng.integers(1, 50, size=src.size), 0)
+    wt = -rng.random(src.size).astype(np.float32)
+    final = np.where(rng.random(N) < 0.5, 0.0, -np.inf).astype(np.float32)
+    g = synth.graph_from_arcs(N, V, src, dst, il, ol, wt, final)
+    B, T = 2, 6
+    lp = np.log(rng.dirichlet(np.ones(V), size=(B, T))).astype(np.float32)
+    lens = np.array([T, 3], np.int32)
+    p = dict(search_beam=30.0, output_beam=5.0, min_active=1, max_active=100, allow_partial=True, lattice=True)
+    G, D = gpu_decoder(W, g, p, B, T)
+    out = D.decode(_cuda(lp), lens)
+    OG = oracle.Graph(g)
+    for b in range(B):
+        ref = oracle_lane(OG, lp[b], lens[b], p)
+        assert_lane_equal(out[b], ref, f"lane {b}")
+        if ref["ok"]:
+            assert_lattice_equal(D.lattice(b), ref["lattice"], f"lane {b}")
+
+
+@pytest.mark.parametrize("start_final", [True, False])
+def test_start_state_without_arcs(W, start_final):
+    """A start state with no arcs: the frontier dies after frame 0; with a
+    final start state the empty path is the result."""
+    N, V = 3, 4
+    src = np.array([1, 2]); dst = np.array([2, 1])
+    il = np.array([1, 2]); ol = np.array([5, 6]); wt = np.array([-0.5, -0.25], np.float32)
+    final = np.array([0.0 if start_final else -np.inf, 0.0, -np.inf], np.float32)
+    g = synth.graph_from_arcs(N, V, src, dst, il, ol, wt, final)
+    rng = np.random.default_rng(3)
+    lp = np.log(rng.dirichlet(np.ones(V), size=(3, 5))).astype(np.float32)
+    lens = np.array([5, 0, 1], np.int32)
+    for allow_partial in (True, False):
+        p = dict(search_beam=10.0, output_beam=3.0, min_active=1, max_active=10, allow_partial=allow_partial,
+                 lattice=True)
+        G, D = gpu_decoder(W, g, p, 3, 5)
+        out = D.decode(_cuda(lp), lens)
+        OG = oracle.Graph(g)
+        for b in range(3):
+            ref = oracle_lane(OG, lp[b], lens[b], p)
+            assert_lane_equal(out[b], ref, f"start_final {start_final} partial {allow_partial} lane {b}")
+        D.close()
+        G.close()
+
+
+def test_all_lengths_zero(W, graphs):
+    wl = synth.workload(0)
+    g = graphs(0)
+    lp = synth.make_log_probs(0, lanes=range(1), T=10)
+    lp = np.concatenate([lp, lp, lp])
+    lens = np.zeros(3, np.int32)
+    p = wl_params(wl)
+    G, D = gpu_decoder(W, g, p, 3, 10)
+    out = D.decode(_cuda(lp), lens)
+    OG = oracle.Graph(g)
+    for b in range(3):
+        assert_lane_equal(out[b], oracle_lane(OG, lp[b], 0, p), f"lane {b}")

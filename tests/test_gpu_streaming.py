@@ -94,3 +94,29 @@ def test_stream_lifecycle_and_chunking_invariance(W):
         assert_lattice_equal(lat16[i], lat, f"lifecycle lattice chunk16 {i}")
     for c in chans:
         D.stream_release(c)
+
+
+def test_workload4_full_128_channels_sampled(W):
+    """The streaming workload in the launch configuration the benchmark times:
+    128 channels, 16-frame chunks, partials every chunk, lattices; sampled
+    channels against the oracle, every channel decoded without overflow."""
+    wl = synth.workload(4)
+    g = synth.make_graph(4)
+    lens = synth.make_lens(4)
+    lp = synth.make_log_probs(4)
+    p = wl_params(wl)
+    G, D = gpu_decoder(W, g, p, wl.B, wl.T, streaming=True)
+    channels = [D.stream_create() for _ in range(wl.B)]
+    partials, final = _run_stream(W, D, lp, lens, wl.chunk, channels)
+    assert all(f["ok"] and f["overflow"] == 0 for f in final)
+    OG = oracle.Graph(g)
+    T = int(lens.max())
+    for i in (5, 77):
+        parts, r, lat = _oracle_stream(OG, p, lp[i], int(lens[i]), wl.chunk, T)
+        for k in (0, len(parts) // 2, len(parts) - 1):
+            assert list(partials[k][i]["words"]) == list(parts[k]["words"]), f"channel {i} chunk {k}"
+            assert abs(partials[k][i]["score"] - parts[k]["score"]) <= SCORE_TOL
+        assert_lane_equal(final[i], r, f"channel {i} final")
+        assert_lattice_equal(D.lattice(channels[i]), lat, f"channel {i} lattice")
+    for c in channels:
+        D.stream_release(c)
