@@ -395,3 +395,36 @@ def test_all_lengths_zero(W, graphs):
     OG = oracle.Graph(g)
     for b in range(3):
         assert_lane_equal(out[b], oracle_lane(OG, lp[b], 0, p), f"lane {b}")
+
+
+def test_work_counters_match_oracle(W, graphs):
+    """The device's work counters (frames, frontier sizes, candidates,
+    admitted, next-frontier sizes, epsilon arcs, arcs expanded) equal the
+    oracle's summed over lanes: the throughput metric and the algorithmic
+    bytes rest on them."""
+    cases = []
+    wl = synth.workload(1)
+    cases.append((graphs(1), synth.make_log_probs(1, lanes=range(4), T=60), np.array([60, 41, 1, 0], np.int32),
+                  wl_params(wl)))
+    wl3 = synth.workload(3)
+    cases.append((graphs(3), synth.make_log_probs(3, lanes=range(2), T=40), np.array([40, 23], np.int32),
+                  wl_params(wl3)))
+    for seed in range(6):
+        g, lp, lens, p = _tiny_case(seed, 0.3)
+        cases.append((g, lp, lens, p))
+    keys = [("frames", "frames"), ("sum_n", "sum_n"), ("sum_D", "sum_D"), ("sum_a", "sum_a"),
+            ("sum_m", "sum_m"), ("eps", "eps_relaxed"), ("arcs_expanded", "arcs_expanded")]
+    for ci, (g, lp, lens, p) in enumerate(cases):
+        G, D = gpu_decoder(W, g, p, len(lens), lp.shape[1])
+        D.decode(_cuda(lp), lens)
+        st = D.stats()
+        OG = oracle.Graph(g)
+        tot = {k: 0 for _, k in keys}
+        for b in range(len(lens)):
+            r = oracle_lane(OG, lp[b], lens[b], p)
+            for _, k in keys:
+                tot[k] += int(r["stats"][k])
+        for gk, ok in keys:
+            assert st[gk] == tot[ok], f"case {ci}: {gk} {st[gk]} vs oracle {ok} {tot[ok]}"
+        D.close()
+        G.close()

@@ -356,3 +356,34 @@ def test_golden_small_cases(case):
         assert r["reached_final"] == case["reached_final"]
         if not case["reached_final"]:
             assert list(part["words"]) == case["words"]
+
+
+def test_work_counters_closed_forms():
+    """The oracle's work counters (they define arcs expanded/s and the
+    algorithmic bytes) on graphs whose counts are fixed by construction."""
+    rng = np.random.default_rng(21)
+    V, T = 9, 30
+    # one final state with V self-loops, beam wide enough to admit everything:
+    # every step has n = 1 token, D = V candidates, a = V admitted, m = 1 state
+    g = synth.graph_from_arcs(1, V, np.zeros(V, np.int64), np.zeros(V, np.int32),
+                              np.arange(V), np.arange(V), np.zeros(V), np.zeros(1))
+    lp = np.log(rng.dirichlet(np.ones(V), size=T)).astype(np.float32)
+    r = oracle.decode(oracle.Graph(g), lp, T, _p(search_beam=1e30, min_active=0, max_active=10**9))
+    st = r["stats"]
+    assert (st["frames"], st["sum_n"], st["sum_D"], st["sum_a"], st["sum_m"]) == (T, T, T * V, T * V, T)
+    assert st["finals"] == 1 and st["eps_relaxed"] == 0
+    assert st["arcs_expanded"] == T * V + 1
+    # a linear chain: one candidate per step, all admitted; no final state
+    N = T + 1
+    src = np.arange(T)
+    g2 = synth.graph_from_arcs(N, V, src, src + 1, rng.integers(1, V, size=T), np.zeros(T, np.int64),
+                               -rng.uniform(0, 1, size=T).astype(np.float32), np.full(N, -np.inf, np.float32))
+    st2 = oracle.decode(oracle.Graph(g2), lp, T, _p(search_beam=1e30))["stats"]
+    assert (st2["sum_n"], st2["sum_D"], st2["sum_a"], st2["sum_m"], st2["finals"]) == (T, T, T, T, 0)
+    # a start state with two epsilon arcs to states with one each (a diamond):
+    # the start closure relaxes 2 + 1 + 1 epsilon arcs, then nothing emits
+    g3 = synth.graph_from_arcs(4, V, np.array([0, 0, 1, 2]), np.array([1, 2, 3, 3]), np.full(4, -1),
+                               np.zeros(4, np.int64), np.array([-1.0, -2.0, -0.5, -0.25], np.float32),
+                               np.array([-np.inf, -np.inf, -np.inf, 0.0], np.float32))
+    st3 = oracle.decode(oracle.Graph(g3), lp, 1, _p(search_beam=1e30))["stats"]
+    assert st3["eps_relaxed"] == 4 and st3["sum_m"] == 0 and st3["finals"] == 0
