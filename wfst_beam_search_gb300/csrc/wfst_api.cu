@@ -568,6 +568,17 @@ static int run_call(wfst_decoder* d, const void* lp, int32_t dtype, int64_t stri
     return fail(WFST_ERR_TIMEOUT, "decode: a device-side grid barrier wait timed out; the call was abandoned");
   }
   if (d->h_bar->error & 2u) return fail(WFST_ERR_CUDA, "decode: epsilon closure did not converge");
+  if (d->h_bar->error & 4u) {
+    // a recombination entry kept changing under a bounded CAS loop: the
+    // affected lanes' results cannot be trusted; their entries are wiped
+    cudaMemsetAsync(d->w.ent, 0, sizeof(ulonglong2) * 2 * L * (size_t)d->w.N, st);
+    cudaStreamSynchronize(st);
+    for (size_t l = 0; l < L; l++) {
+      d->chan_state[l] = 0;
+      d->lat_valid[l] = 0;
+    }
+    return fail(WFST_ERR_TIMEOUT, "decode: a recombination CAS loop gave up after its retry bound");
+  }
   float ms = 0.f;
   cudaEventElapsedTime(&ms, d->ev0, d->ev1);
   // per-call counters

@@ -290,6 +290,8 @@ extern "C" int wfst_decode_static(const wfst_graph* g, const wfst_params* params
   if (bar.error & 1u)
     return api_fail(WFST_ERR_TIMEOUT, "decode_static: a device-side grid barrier wait timed out; the call was abandoned");
   if (bar.error & 2u) return api_fail(WFST_ERR_CUDA, "decode_static: epsilon closure did not converge");
+  if (bar.error & 4u)
+    return api_fail(WFST_ERR_TIMEOUT, "decode_static: a recombination CAS loop gave up after its retry bound");
   for (int32_t b = 0; b < B; b++) {
     const Result& r = res[b];
     const int32_t nw = r.ok ? r.n_words : 0;
