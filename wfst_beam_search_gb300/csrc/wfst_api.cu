@@ -414,6 +414,7 @@ extern "C" int wfst_decoder_create(wfst_graph* g, const wfst_params* params, int
     DA(w.lat_out_n, L, true);
   }
   DA(w.path, L * path_cap, false);
+  DA(w.pframe, L * (size_t)mf, false);
   DA(w.res, L, true);
   DA(w.bar, 1, true);
   DA(w.prof, kProfSlots, true);

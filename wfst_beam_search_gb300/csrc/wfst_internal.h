@@ -72,6 +72,8 @@ struct LaneState {                // persistent per lane (mirrored in shared mem
   uint32_t eps_pass;              // epsilon worklist pass id (dedupe marks)
   int32_t overflow;
   int32_t t_eff;                  // offline length (last-frames rule), -1 streaming
+  int32_t bt_top;                 // frame of the last backtracked path's newest token, -1 = none
+  int32_t bt_len;                 // arcs of that path (kept oldest-first in path)
   int32_t pad;
 };
 
@@ -148,7 +150,8 @@ struct DevWork {
   uint32_t* bwd;                  // [L][log_cap] ordered backward scores
   LatRec* lat_out;                // [L][lat_cap] kept records (compacted)
   unsigned long long* lat_out_n;  // [L]
-  int32_t* path;                  // [L][path_cap]
+  int32_t* path;                  // [L][path_cap] best path, oldest arc first (the tail is walk scratch)
+  int2* pframe;                   // [L][max_frames+2] per frame of that path: {winners-log index, path position}
   Result* res;                    // [L]
   int32_t* words;                 // [L][words_cap] (words_cap per call)
   GridBar* bar;

@@ -81,6 +81,7 @@ struct Smem {
   unsigned long long prof[kProfSlots + 2];  // CTA 0's phase timers + two time marks
   int64_t bt_idx;
   int32_t bt_ok, bt_reached, bt_state, bt_pad;
+  int32_t bt_d, bt_lo, bt_hi;
   float bt_score;
 };
 
@@ -752,6 +753,8 @@ __device__ void init_lane_global(const RunArgs& a, int l) {
     w.lat_out_n[l] = 0ull;
   }
   w.lanes[l].overflow = 0;
+  w.lanes[l].bt_top = -1;  // no path to continue from
+  w.lanes[l].bt_len = 0;
   const int32_t s0 = g.start;
   const int4 m = __ldg(g.meta + s0);
   const uint32_t deg = (uint32_t)(m.y - m.x);
@@ -1365,21 +1368,49 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
           if (pos < 0) ok = 0;
           int64_t idx = -1;
           if (ok) idx = s.base_cur + pos;
-          // walk the winners chain; the newest arc lands at the end of the buffer
+          // Walk the winners chain from the newest arc back, writing the arcs
+          // newest-first into the tail of the path buffer.  The previous
+          // backtrack of this lane (an earlier partial, §8) left its path
+          // oldest-first at the head, with each frame's first entry in pframe:
+          // once this walk meets that entry the two paths are the same from
+          // there back to the start, and the walk stops.
           int64_t n = 0;
           int32_t* path = w.path + (size_t)l * w.path_cap;
+          int2* pf = w.pframe + (size_t)l * (w.max_frames + 2);
           const int2* lg = w.wlog + (size_t)l * w.log_cap;
+          const int prev_top = __ldcg(&w.lanes[l].bt_top);
+          int32_t d = -1;  // path position of the meeting entry (-1: the walk reached the start)
+          int32_t fr = f, fr_seen = f + 1;
           int64_t i = idx;
           const int64_t limit = min(s.cursor, w.log_cap);
           while (ok && i >= 0 && i < limit && n <= limit) {
+            // (frames past the table, possible on a long stream, are simply
+            // not recorded: the walk meets the earlier path at a later check)
+            if (fr != fr_seen) {  // the first entry of frame fr on this walk
+              const bool in_table = fr >= 0 && fr <= w.max_frames + 1;
+              if (in_table && fr <= prev_top) {
+                const int2 pe = __ldcg(pf + fr);
+                if (pe.x == (int32_t)i) { d = pe.y; break; }
+              }
+              if (in_table) pf[fr] = make_int2((int32_t)i, (int32_t)n);
+              fr_seen = fr;
+            }
             const int2 e = __ldcg(lg + i);
             if (e.y < 0) break;
             if (n < w.path_cap) path[w.path_cap - 1 - n] = e.y;
             n++;
+            if (!(__ldg(g.c_src + e.y) >> 31)) fr--;  // an emitting arc ends one frame later
             i = e.x;
           }
-          if (n > w.path_cap) lane_ovf(a, l, kOvfPath);
-          S.bt_n = (int32_t)min(n, w.path_cap);
+          const int64_t len = (int64_t)d + 1 + n;
+          if (n > w.path_cap || len + n > w.path_cap) {
+            lane_ovf(a, l, kOvfPath);
+            ok = 0;
+          }
+          S.bt_n = (int32_t)n;
+          S.bt_d = d;
+          S.bt_lo = fr_seen;  // frames [fr_seen, f] were recorded by this walk
+          S.bt_hi = f;
           S.bt_ok = ok;
           S.bt_reached = reached;
           S.bt_score = ok ? score : -INFINITY;
@@ -1399,9 +1430,31 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
           }
         }
         __syncthreads();
+        {  // splice: the walk's arcs go after the shared prefix, oldest first;
+           // the recorded frames get their final path positions
+          const int nw = S.bt_n, dd = S.bt_d;
+          int32_t* path = w.path + (size_t)l * w.path_cap;
+          int2* pf = w.pframe + (size_t)l * (w.max_frames + 2);
+          if (S.bt_ok) {
+            for (int k = tid; k < nw; k += kThreads) path[dd + nw - k] = path[w.path_cap - 1 - k];
+            const int fr_hi = min(S.bt_hi, w.max_frames + 1);
+            for (int fr = max(S.bt_lo, 0) + tid; fr <= fr_hi; fr += kThreads) {
+              int2 e = pf[fr];
+              e.y = dd + nw - e.y;
+              pf[fr] = e;
+            }
+          }
+          __syncthreads();
+          if (tid == 0) {
+            w.lanes[l].bt_top = S.bt_ok ? S.bt_hi : -1;
+            w.lanes[l].bt_len = S.bt_ok ? dd + 1 + nw : 0;
+            S.bt_n = S.bt_ok ? dd + 1 + nw : 0;
+          }
+          __syncthreads();
+        }
         // words = the path's non-zero output labels, forward order
         const int n = S.bt_n;
-        const int32_t* path = w.path + (size_t)l * w.path_cap + (w.path_cap - n);
+        const int32_t* path = w.path + (size_t)l * w.path_cap;
         int32_t* out = w.words + (size_t)l * a.words_cap;
         int run = 0;
         for (int base = 0; base < n; base += kThreads) {

@@ -152,6 +152,7 @@ size_t layout(unsigned char* base, const DevGraph& G, int L, int T, const wfst_p
   }
   w.wlog = c.take<int2>((size_t)L * w.log_cap);
   w.path = c.take<int32_t>((size_t)L * w.path_cap);
+  w.pframe = c.take<int2>((size_t)L * mf);
   w.words = c.take<int32_t>((size_t)L * words_cap);
   return (c.off + 255) & ~(size_t)255;
 }
