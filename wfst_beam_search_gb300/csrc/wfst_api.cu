@@ -307,19 +307,20 @@ static cudaError_t dalloc(wfst_decoder* d, T** p, size_t n, bool zero = false) {
   return e;
 }
 
-// Replace one workspace array by a fresh one of n elements (contents lost).
-template <typename T>
-static cudaError_t dregrow(wfst_decoder* d, T** p, size_t n) {
+// Swap a workspace array for a freshly allocated one (old contents dropped).
+static void dswap(wfst_decoder* d, void** slot, void* fresh, size_t bytes) {
   for (size_t i = 0; i < d->allocs.size(); i++) {
-    if (d->allocs[i] != (void*)*p) continue;
-    cudaFree(*p);
+    if (d->allocs[i] != *slot) continue;
+    cudaFree(*slot);
     d->bytes -= (int64_t)d->alloc_bytes[i];
     d->allocs.erase(d->allocs.begin() + (long)i);
     d->alloc_bytes.erase(d->alloc_bytes.begin() + (long)i);
     break;
   }
-  *p = nullptr;
-  return dalloc(d, p, n, false);
+  *slot = fresh;
+  d->allocs.push_back(fresh);
+  d->alloc_bytes.push_back(bytes);
+  d->bytes += (int64_t)bytes;
 }
 
 static void decoder_destroy(wfst_decoder* d) {
@@ -636,44 +637,53 @@ static void write_lane(wfst_decoder* d, int32_t lane, int32_t out_index, int32_t
 }
 
 // Offline capacity growth: double the capacity behind each overflow seen
-// (winners log, lattice arena, frontier up to num_states, best path) and
-// reallocate those arrays.  WFST_ERR_CAPACITY when nothing can grow.
+// (winners log, lattice arena, frontier up to num_states, best path up to the
+// longest path a decode can have).  Every new array is allocated before any
+// old one is released, so a failed allocation leaves the decoder as it was.
+// WFST_ERR_CAPACITY when nothing can grow (sizes at their bounds, or device
+// memory exhausted): the lanes keep their overflow bits.
 static int grow_capacities(wfst_decoder* d, bool g_log, bool g_lat, bool g_q, bool g_path) {
   DevWork& w = d->w;
   const size_t L = (size_t)d->L;
   const DevGraph& G = d->g->dg;
-  bool any = false;
-  cudaError_t e = cudaSuccess;
+  struct Plan { void** slot; size_t bytes; void* fresh; };
+  Plan plan[8];
+  int np = 0;
+  int64_t log_cap = w.log_cap, lat_cap = w.lat_cap, qcap = w.qcap, path_cap = w.path_cap;
+  const int64_t path_bound = 2 * ((int64_t)d->max_frames + 2) * (1 + (int64_t)G.eps_depth);
   if (g_log && w.log_cap < (int64_t)INT32_MAX - 1) {
-    w.log_cap = std::min<int64_t>(2 * w.log_cap, (int64_t)INT32_MAX - 1);
-    e = dregrow(d, &w.wlog, L * (size_t)w.log_cap);
-    if (e == cudaSuccess && w.lattice) e = dregrow(d, &w.bwd, L * (size_t)w.log_cap);
-    any = true;
+    log_cap = std::min<int64_t>(2 * w.log_cap, (int64_t)INT32_MAX - 1);
+    plan[np++] = {(void**)&w.wlog, sizeof(int2) * L * (size_t)log_cap, nullptr};
+    if (w.lattice) plan[np++] = {(void**)&w.bwd, sizeof(uint32_t) * L * (size_t)log_cap, nullptr};
   }
-  if (e == cudaSuccess && g_lat && w.lattice && w.lat_cap < ((int64_t)1 << 40)) {
-    w.lat_cap *= 2;
-    e = dregrow(d, &w.lat, L * (size_t)w.lat_cap);
-    if (e == cudaSuccess) e = dregrow(d, &w.lat_out, L * (size_t)w.lat_cap);
-    any = true;
+  if (g_lat && w.lattice && w.lat_cap < ((int64_t)1 << 40)) {
+    lat_cap = 2 * w.lat_cap;
+    plan[np++] = {(void**)&w.lat, sizeof(LatRec) * L * (size_t)lat_cap, nullptr};
+    plan[np++] = {(void**)&w.lat_out, sizeof(LatRec) * L * (size_t)lat_cap, nullptr};
   }
-  if (e == cudaSuccess && g_q && w.qcap < (int64_t)G.N) {
-    w.qcap = std::min<int64_t>(2 * w.qcap, (int64_t)G.N);
-    e = dregrow(d, &w.front, 2 * L * (size_t)w.qcap);
-    if (e == cudaSuccess) e = dregrow(d, &w.score, 2 * L * (size_t)w.qcap);
-    if (e == cudaSuccess && G.has_eps) e = dregrow(d, &w.wl, 2 * L * (size_t)w.qcap);
-    any = true;
+  if (g_q && w.qcap < (int64_t)G.N) {
+    qcap = std::min<int64_t>(2 * w.qcap, (int64_t)G.N);
+    plan[np++] = {(void**)&w.front, sizeof(TokRec) * 2 * L * (size_t)qcap, nullptr};
+    plan[np++] = {(void**)&w.score, sizeof(float) * 2 * L * (size_t)qcap, nullptr};
+    if (G.has_eps) plan[np++] = {(void**)&w.wl, sizeof(TokRec) * 2 * L * (size_t)qcap, nullptr};
   }
-  if (e == cudaSuccess && g_path && w.path_cap < (int64_t)INT32_MAX / 2) {
-    w.path_cap = std::min<int64_t>(2 * w.path_cap, (int64_t)INT32_MAX / 2);
-    e = dregrow(d, &w.path, L * (size_t)w.path_cap);
-    any = true;
+  if (g_path && w.path_cap < path_bound) {
+    path_cap = std::min<int64_t>(2 * w.path_cap, path_bound);
+    plan[np++] = {(void**)&w.path, sizeof(int32_t) * L * (size_t)path_cap, nullptr};
   }
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return e == cudaErrorMemoryAllocation ? fail(WFST_ERR_OOM, "decode: out of device memory while growing capacities")
-                                          : cuda_fail(e, "decode: capacity growth");
+  if (np == 0) return fail(WFST_ERR_CAPACITY, "decode: capacities are at their bounds");
+  for (int i = 0; i < np; i++) {
+    if (cudaMalloc(&plan[i].fresh, plan[i].bytes) != cudaSuccess) {
+      cudaGetLastError();
+      for (int k = 0; k < i; k++) cudaFree(plan[k].fresh);
+      return fail(WFST_ERR_CAPACITY, "decode: no device memory to grow capacities");
+    }
   }
-  if (!any) return fail(WFST_ERR_CAPACITY, "decode: capacities are at their largest");
+  for (int i = 0; i < np; i++) dswap(d, plan[i].slot, plan[i].fresh, plan[i].bytes);
+  w.log_cap = log_cap;
+  w.lat_cap = lat_cap;
+  w.qcap = qcap;
+  w.path_cap = path_cap;
   d->grows++;
   return WFST_OK;
 }

@@ -51,6 +51,7 @@ struct SmLane {
   unsigned long long frames, sum_n, sum_d, sum_m;
   float maxlp, prev_max;          // max log-prob of frame t; the previous step's max end
   int32_t has_prev, was_emit;
+  int32_t prev_cleared;           // the previous frame's entries were cleared by its expand pass
 };
 
 struct WStage {                   // one warp's staged tokens of its current tile
@@ -459,7 +460,10 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
     const int ntiles = S.pre_a[l + 1] - S.pre_a[l];
     const uint32_t s_lo = (uint32_t)k * kTile;
     const uint32_t s_hi = min(s_lo + (uint32_t)kTile, s.d_cur);
-    const int32_t p_lo = __ldcg(w.tile_first + tl(w, par, l) + k);
+    // tokens [p_lo, p_hi) hold this tile's slots; the expand pass also stages
+    // the arc-less tokens before the first slot, so that every token of the
+    // frame is staged (and its entry cleared) once at least
+    const int32_t p_lo = (MODE == 1 && k == 0) ? 0 : __ldcg(w.tile_first + tl(w, par, l) + k);
     int32_t p_hi = (k + 1 < ntiles) ? __ldcg(w.tile_first + tl(w, par, l) + k + 1) + 1 : s.n_cur;
     if (p_hi > s.n_cur) p_hi = s.n_cur;
     const LP* row = lpb + (int64_t)s.row * a.stride_b + (int64_t)(f - s.t0) * a.stride_t;
@@ -488,6 +492,9 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
             w.score[q + c + i] = sc;
           } else {
             sc = __ldcg(w.score + q + c + i);
+            // the frame's entries were last read in phase X: clear this one
+            // now, while its line is likely still in L2
+            *ent_at(w, l, tr.state, par) = make_ulonglong2(0ull, 0ull);
           }
           ws.off[i] = tr.off;
           ws.row[i] = tr.row;
@@ -977,6 +984,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     s.closure = 0;
     s.cutoff = 0.f;
     s.n_cur = s.n_prev = 0;
+    s.prev_cleared = 0;  // not known at launch: the first step clears as well
     s.d_cur = 0;
     if (s.flags & kCallInit) {
       s.t = 0;
@@ -1079,7 +1087,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         s.prev_max = pk ? unord_f(pk) : -INFINITY;
       }
       S.pre_b[l] = (s.need_commit || s.phase == kFin || s.phase == kPart) ? s.n_cur : 0;
-      S.pre_c[l] = s.n_prev;
+      // the previous frame's entries, unless its expand pass cleared them
+      S.pre_c[l] = s.prev_cleared ? 0 : s.n_prev;
       if (lat && s.need_commit) {
         // records appended since frame t-1's commit: emit(t-1) and eps(t)
         // (for t = 0: the start closure's records)
@@ -1516,9 +1525,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     for (int l = tid; l < L; l += kThreads) {
       SmLane& s = S.lane[l];
       s.was_emit = 0;
+      s.prev_cleared = 0;
       if (s.phase == kEmit) {
         s.t += 1;
         s.was_emit = 1;
+        s.prev_cleared = s.expanded;  // the expand pass staged, and cleared, every token
       } else if (s.phase == kFin) {
         s.done_final = 1;
         s.status = kLaneDone;
