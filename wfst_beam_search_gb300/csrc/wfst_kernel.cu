@@ -51,6 +51,8 @@ struct SmLane {
   unsigned long long frames, sum_n, sum_d, sum_m;
   float maxlp, prev_max;          // max log-prob of frame t; the previous step's max end
   int32_t has_prev, was_emit;
+  float cur_max;                  // this step's exact max end (expand pass)
+  int32_t seed_next;              // the expand pass seeds the next step's max
   int32_t prev_cleared;           // the previous frame's entries were cleared by its expand pass
 };
 
@@ -460,11 +462,13 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
     const int ntiles = S.pre_a[l + 1] - S.pre_a[l];
     const uint32_t s_lo = (uint32_t)k * kTile;
     const uint32_t s_hi = min(s_lo + (uint32_t)kTile, s.d_cur);
-    // tokens [p_lo, p_hi) hold this tile's slots; the expand pass also stages
-    // the arc-less tokens before the first slot, so that every token of the
-    // frame is staged (and its entry cleared) once at least
-    const int32_t p_lo = (MODE == 1 && k == 0) ? 0 : __ldcg(w.tile_first + tl(w, par, l) + k);
-    int32_t p_hi = (k + 1 < ntiles) ? __ldcg(w.tile_first + tl(w, par, l) + k + 1) + 1 : s.n_cur;
+    // tokens [p_lo, p_hi) hold this tile's slots (tile 0 also takes the
+    // arc-less tokens before the first slot); the tile owns [p_lo, own_hi):
+    // every token of the frame is owned by exactly one tile, which commits it
+    // in the max pass; the expand pass clears every staged token's entry
+    const int32_t p_lo = (k == 0) ? 0 : __ldcg(w.tile_first + tl(w, par, l) + k);
+    const int32_t own_hi = (k + 1 < ntiles) ? __ldcg(w.tile_first + tl(w, par, l) + k + 1) : s.n_cur;
+    int32_t p_hi = (k + 1 < ntiles) ? own_hi + 1 : s.n_cur;
     if (p_hi > s.n_cur) p_hi = s.n_cur;
     const LP* row = lpb + (int64_t)s.row * a.stride_b + (int64_t)(f - s.t0) * a.stride_t;
     const size_t q = ql(w, par, l);
@@ -488,8 +492,25 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
           const TokRec tr = ld_tok(w.front + q + c + i);
           float sc;
           if (MODE == 0) {
-            sc = key_score(__ldcg(&ent_at(w, l, tr.state, par)->x));
+            const ulonglong2 e = __ldcg(ent_at(w, l, tr.state, par));
+            sc = key_score(e.x);
             w.score[q + c + i] = sc;
+            const int32_t p = c + i;
+            if (s.need_commit && p < own_hi) {
+              // commit (§5.4): the winners-log entry {prev, arc} of the token
+              const int32_t arc = key_id(e.x);
+              const uint32_t src = ent_src(e);
+              const int64_t base_new = s.cursor, base_old = s.base_cur;
+              const int32_t prev =
+                  arc < 0 ? -1 : (int32_t)(((src >> 31) ? base_new : base_old) + (src & 0x7fffffffu));
+              const int64_t idx = base_new + p;
+              if (idx < w.log_cap) w.wlog[(size_t)l * w.log_cap + idx] = make_int2(prev, arc);
+              else lane_ovf(a, l, kOvfArena);
+              if (g.has_eps) {
+                const int4 m = __ldg(g.meta + tr.state);
+                if (m.z > m.y) atomicAdd(&w.stats[l].eps, (unsigned long long)(m.z - m.y));
+              }
+            }
           } else {
             sc = __ldcg(w.score + q + c + i);
             // the frame's entries were last read in phase X: clear this one
@@ -553,6 +574,30 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
         for (int j = 0; j < kSPT; j++) {
           adm[j] = act[j] && (end[j] > thr);
           if (!adm[j]) d[j] = id[j] = 0;
+        }
+        if (s.seed_next) {
+          // an arc that attains this step's max makes its destination a best
+          // token of the next frame: one chunk of that state's arcs posts an
+          // achieved end of the next step before its max pass (§5.3
+          // upper-bound skip) begins
+          const LP* nrow = row + a.stride_t;
+#pragma unroll
+          for (int j = 0; j < kSPT; j++) {
+            unsigned m32 = __ballot_sync(0xffffffffu, adm[j] && end[j] == s.cur_max);
+            while (m32) {
+              const int sl = __ffs(m32) - 1;
+              m32 &= m32 - 1;
+              const int32_t dd = __shfl_sync(0xffffffffu, d[j], sl);
+              const float e0 = __shfl_sync(0xffffffffu, end[j], sl);
+              const int4 m = __ldg(g.meta + dd);
+              const int32_t ai = m.x + lane;
+              float mx = -INFINITY;
+              if (ai < m.y)
+                mx = __fadd_rn(__fadd_rn(e0, __ldg(g.weight + ai)), lp_at<LP>(nrow, __ldg(g.ilabel + ai)));
+              for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+              if (lane == 0 && mx > -INFINITY) atomicMax(&fc_of(w, f + 1, l)->maxkey, ord_f(mx));
+            }
+          }
         }
         if (a.lattice) {
 #pragma unroll
@@ -1086,7 +1131,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         s.has_prev = pk != 0u;
         s.prev_max = pk ? unord_f(pk) : -INFINITY;
       }
-      S.pre_b[l] = (s.need_commit || s.phase == kFin || s.phase == kPart) ? s.n_cur : 0;
+      // the commit loop: final / partial lanes, and frames without emitting
+      // arcs (no tiles); the max pass commits every other frame
+      S.pre_b[l] = (s.phase == kFin || s.phase == kPart || (s.need_commit && s.d_cur == 0)) ? s.n_cur : 0;
       // the previous frame's entries, unless its expand pass cleared them
       S.pre_c[l] = s.prev_cleared ? 0 : s.n_prev;
       if (lat && s.need_commit) {
@@ -1281,6 +1328,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         const unsigned mk = __ldcg(&fc_of(w, s.t, l)->maxkey);
         s.expanded = mk != 0u;
         s.cutoff = mk ? __fsub_rn(unord_f(mk), s.beam) : INFINITY;
+        s.cur_max = mk ? unord_f(mk) : -INFINITY;
+        s.seed_next = (a.ub_skip && mk && s.t + 1 < s.t_end) ? 1 : 0;
         if (s.expanded) S.pre_a[l] = (int32_t)((s.d_cur + kTile - 1) / kTile);
       }
     }
