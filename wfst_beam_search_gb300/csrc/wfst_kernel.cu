@@ -49,8 +49,8 @@ struct SmLane {
   int32_t wl_n, closure;
   int64_t res_lo, res_hi;         // lattice records resolved in this step's commit phase
   unsigned long long frames, sum_n, sum_d, sum_m;
-  float maxlp, prev_max;          // max log-prob of frame t; the previous step's max end
-  int32_t has_prev, was_emit;
+  float maxlp;                    // max log-prob of frame t
+  int32_t was_emit;
   float cur_max;                  // this step's exact max end (expand pass)
   int32_t seed_next;              // the expand pass seeds the next step's max
   int32_t prev_cleared;           // the previous frame's entries were cleared by its expand pass
@@ -169,6 +169,37 @@ __device__ __forceinline__ int find_tok(const uint32_t* off, int n, uint32_t slo
 __device__ void lane_scan(int32_t* pre, int L) {
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
+    const int per = (L + 31) / 32;
+    int32_t local = 0;
+    for (int i = 0; i < per; i++) {
+      const int idx = lane * per + i;
+      if (idx < L) local += pre[idx];
+    }
+    int32_t inc = local;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += v;
+    }
+    int32_t run = inc - local;
+    for (int i = 0; i < per; i++) {
+      const int idx = lane * per + i;
+      if (idx < L) {
+        const int32_t v = pre[idx];
+        pre[idx] = run;
+        run += v;
+      }
+    }
+    if (lane == 31) pre[L] = inc;
+  }
+  __syncthreads();
+}
+
+// lane_scan of four arrays at once (warp w scans array w), one barrier.
+__device__ void lane_scan4(int32_t* p0, int32_t* p1, int32_t* p2, int32_t* p3, int L) {
+  const int warp = threadIdx.x >> 5;
+  if (warp < 4) {
+    int32_t* pre = warp == 0 ? p0 : warp == 1 ? p1 : warp == 2 ? p2 : p3;
+    const int lane = threadIdx.x & 31;
     const int per = (L + 31) / 32;
     int32_t local = 0;
     for (int i = 0; i < per; i++) {
@@ -1127,9 +1158,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         s.sum_n += n_raw;
         s.sum_d += s.d_cur;
         s.maxlp = __ldcg(w.maxlp + (size_t)l * w.max_frames + (s.t - s.t0));
-        const unsigned pk = s.t >= 1 ? __ldcg(&fc_of(w, s.t - 1, l)->maxkey) : 0u;
-        s.has_prev = pk != 0u;
-        s.prev_max = pk ? unord_f(pk) : -INFINITY;
       }
       // the commit loop: final / partial lanes, and frames without emitting
       // arcs (no tiles); the max pass commits every other frame
@@ -1145,19 +1173,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         S.pre_d[l] = (int32_t)(s.res_hi - s.res_lo);
       }
     }
-    __syncthreads();
-    if (tid == 0) {
-      int any = 0;
-      for (int l = 0; l < L; l++) any |= S.lane[l].phase;
-      S.any = any;
-    }
-    __syncthreads();
-    if (!S.any) break;
+    int any_active = 0;
+    for (int l = tid; l < L; l += kThreads) any_active |= S.lane[l].phase;
+    if (!__syncthreads_or(any_active)) break;
     steps++;
-    lane_scan(S.pre_a, L);
-    lane_scan(S.pre_b, L);
-    lane_scan(S.pre_c, L);
-    lane_scan(S.pre_d, L);
+    lane_scan4(S.pre_a, S.pre_b, S.pre_c, S.pre_d, L);
     prof_mark(prof, tsub, kProfPrologue);
 
     // ================= phase X: commit frame t, clear frame t-1, exact max
@@ -1174,18 +1194,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
           w.lat_groups[(size_t)l * (w.max_frames + 2) + s.t] = s.res_hi;
       }
     }
-    {  // commit (§5.4): winners-log entry {prev, arc} per token; final-step
-       // keys; a best token of an emitting lane seeds the exact max
+    {  // commit (§5.4) of final / partial lanes and of frames without
+       // emitting arcs: winners-log entry {prev, arc} per token; final-step
+       // keys and the best token
       const int total = S.pre_b[L];
       const int wlane = tid & 31;
-      // warp-uniform trip count: the seed below is a warp-collective
       // every CTA takes an equal contiguous share (one batch per thread when
       // the frame fits G * kThreads * kCB tokens)
       const int per = (total + G - 1) / G;
       const int c0 = min(total, blockIdx.x * per), c1 = min(total, c0 + per);
       for (int wb = c0 + (tid & ~31); wb < c1; wb += kThreads * kCB) {
         const int g0 = wb + wlane;
-        unsigned seed = 0;  // bit k: token k of this thread seeds the max
         int lk[kCB];
         int32_t pk[kCB], st[kCB];
         bool v[kCB];
@@ -1235,30 +1254,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
             }
           }
           if (s.phase == kFin || s.phase == kPart) atomicMax(&fc_of(w, f, l)->best_key, key[k]);
-          if (s.phase == kEmit && a.ub_skip && s.has_prev && score == s.prev_max) seed |= 1u << k;
-        }
-        // a best token of the frame: its arcs give an achieved end early; the
-        // warp walks them together
-#pragma unroll
-        for (int k = 0; k < kCB; k++) {
-          unsigned m32 = __ballot_sync(0xffffffffu, (seed >> k) & 1u);
-          while (m32) {
-            const int src = __ffs(m32) - 1;
-            m32 &= m32 - 1;
-            const int l = __shfl_sync(0xffffffffu, lk[k], src);
-            const int32_t state = __shfl_sync(0xffffffffu, st[k], src);
-            const float score = __shfl_sync(0xffffffffu, key_score(key[k]), src);
-            const SmLane& s = S.lane[l];
-            const int4 m = __ldg(g.meta + state);
-            const LP* row = lpb + (int64_t)s.row * a.stride_b + (int64_t)(s.t - s.t0) * a.stride_t;
-            float mx = -INFINITY;
-            for (int32_t ai = m.x + wlane; ai < m.y; ai += 32)
-              mx = fmaxf(mx, __fadd_rn(__fadd_rn(score, __ldg(g.weight + ai)),
-                                       lp_at<LP>(row, __ldg(g.ilabel + ai))));
-#pragma unroll
-            for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            if (wlane == 0 && mx > -INFINITY) atomicMax(&fc_of(w, s.t, l)->maxkey, ord_f(mx));
-          }
         }
       }
     }
