@@ -151,7 +151,6 @@ extern "C" int wfst_graph_upload(const wfst_graph_desc* d, int32_t device, wfst_
   std::vector<uint16_t> il16(A ? A : 1);
   std::vector<float> wt(A ? A : 1);
   std::vector<int32_t> dst(A ? A : 1), aid(A ? A : 1), csrc(A ? A : 1);
-  bool identity = true;
   for (int64_t s = 0; s < N; s++) {
     int64_t k = rs[s];
     float maxw = -INFINITY;
@@ -163,7 +162,6 @@ extern "C" int wfst_graph_upload(const wfst_graph_desc* d, int32_t device, wfst_
         wt[k] = d->weight[a];
         dst[k] = d->dst[a];
         aid[k] = (int32_t)a;
-        if (k != a) identity = false;
         if (!eps) maxw = std::max(maxw, d->weight[a]);
         k++;
       }
@@ -189,22 +187,13 @@ extern "C" int wfst_graph_upload(const wfst_graph_desc* d, int32_t device, wfst_
   G.has_eps = has_eps ? 1 : 0;
   G.A = A;
   G.eps_depth = eps_depth;
-  G.identity = identity ? 1 : 0;
   cudaError_t e = cudaSuccess;
   int4* p_meta;
-  uint16_t* p_il;
-  float *p_w, *p_fin;
-  int32_t *p_dst, *p_aid = nullptr, *p_csrc, *p_cdst, *p_col;
+  float* p_fin;
+  int32_t *p_csrc, *p_cdst, *p_col;
   if (e == cudaSuccess) e = dev_upload(&p_meta, meta.data(), N, g->allocs, g->bytes);
-  if (e == cudaSuccess) e = dev_upload(&p_il, il16.data(), A, g->allocs, g->bytes);
-  if (e == cudaSuccess) e = dev_upload(&p_w, wt.data(), A, g->allocs, g->bytes);
-  if (e == cudaSuccess) e = dev_upload(&p_dst, dst.data(), A, g->allocs, g->bytes);
-  if (e == cudaSuccess && !identity) e = dev_upload(&p_aid, aid.data(), A, g->allocs, g->bytes);
   if (e == cudaSuccess) e = dev_upload(&p_csrc, csrc.data(), A, g->allocs, g->bytes);
-  if (e == cudaSuccess) {
-    if (identity) p_cdst = p_dst;
-    else e = dev_upload(&p_cdst, d->dst, A, g->allocs, g->bytes);
-  }
+  if (e == cudaSuccess) e = dev_upload(&p_cdst, d->dst, A, g->allocs, g->bytes);
   if (e == cudaSuccess) e = dev_upload(&p_col, d->olabel, A, g->allocs, g->bytes);
   if (e == cudaSuccess) e = dev_upload(&p_fin, d->final_weight, N, g->allocs, g->bytes);
   int4* p_arcs = nullptr;
@@ -223,10 +212,6 @@ extern "C" int wfst_graph_upload(const wfst_graph_desc* d, int32_t device, wfst_
                                           : cuda_fail(e, "graph_upload");
   }
   G.meta = p_meta;
-  G.ilabel = p_il;
-  G.weight = p_w;
-  G.dst = p_dst;
-  G.arc_id = p_aid;
   G.c_src = p_csrc;
   G.c_dst = p_cdst;
   G.c_olabel = p_col;

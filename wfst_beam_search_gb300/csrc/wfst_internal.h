@@ -39,13 +39,9 @@ struct DevGraph {
   int32_t N, start, V, has_eps;
   int64_t A;
   int32_t eps_depth;              // longest epsilon path (passes needed by a closure)
-  int32_t identity;               // internal arc order == caller arc order
+  int32_t pad;
   const int4* meta;               // [N] {row_begin, emit_end, eps_end, emit_maxw bits}
-  const uint16_t* ilabel;         // [A] internal, 0xFFFF on epsilon arcs
-  const float* weight;            // [A] internal
-  const int32_t* dst;             // [A] internal
-  const int32_t* arc_id;          // [A] internal -> caller id (nullptr when identity)
-  const int4* arcs;               // [A] internal {dst, weight bits, ilabel, caller id}: expand pass
+  const int4* arcs;               // [A] internal {dst, weight bits, ilabel (-1 = epsilon), caller id}
   const int32_t* c_src;           // [A] caller id -> src state | (epsilon << 31)
   const int32_t* c_dst;           // [A] caller id -> dst state
   const int32_t* c_olabel;        // [A] caller id -> olabel

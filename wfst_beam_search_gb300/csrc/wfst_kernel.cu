@@ -570,16 +570,17 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
         if (act[j] && a.ub_skip && ws.ub[ti[j]] <= thr) act[j] = false;
         ai[j] = act[j] ? ws.row[ti[j]] + (int32_t)(slot - ws.off[ti[j]]) : 0;
       }
-      // the max pass reads the ilabel/weight columns; the expand pass reads one
-      // 16-byte record per arc {dst, weight, ilabel, arc id} (one vector load)
+      // one 16-byte record per arc {dst, weight, ilabel, arc id} (one vector
+      // load); the expand pass finds the max pass's lines still in L2
       int il[kSPT];
       float wt[kSPT];
       int32_t d[kSPT], id[kSPT];
 #pragma unroll
       for (int j = 0; j < kSPT; j++) {
         if (MODE == 0) {
-          il[j] = act[j] ? (int)__ldg(g.ilabel + ai[j]) : 0;
-          wt[j] = act[j] ? __ldg(g.weight + ai[j]) : 0.f;
+          const int4 r = act[j] ? __ldg(g.arcs + ai[j]) : make_int4(0, 0, 0, 0);
+          il[j] = r.z;
+          wt[j] = __int_as_float(r.y);
           d[j] = id[j] = 0;
         } else {
           const int4 r = act[j] ? __ldg(g.arcs + ai[j]) : make_int4(0, 0, 0, 0);
@@ -623,8 +624,10 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
               const int4 m = __ldg(g.meta + dd);
               const int32_t ai = m.x + lane;
               float mx = -INFINITY;
-              if (ai < m.y)
-                mx = __fadd_rn(__fadd_rn(e0, __ldg(g.weight + ai)), lp_at<LP>(nrow, __ldg(g.ilabel + ai)));
+              if (ai < m.y) {
+                const int4 r = __ldg(g.arcs + ai);
+                mx = __fadd_rn(__fadd_rn(e0, __int_as_float(r.y)), lp_at<LP>(nrow, r.z));
+              }
               for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
               if (lane == 0 && mx > -INFINITY) atomicMax(&fc_of(w, f + 1, l)->maxkey, ord_f(mx));
             }
@@ -1028,7 +1031,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
   const int64_t gstride = (int64_t)G * kThreads;
   const int64_t gstart = (int64_t)blockIdx.x * kThreads + tid;
   const bool lat = a.lattice != 0;
-  const LP* lpb = reinterpret_cast<const LP*>(a.lp);
   unsigned epoch = 0;
   unsigned long long steps = 0;
   unsigned long long* prof = S.prof;
