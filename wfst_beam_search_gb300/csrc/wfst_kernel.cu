@@ -81,6 +81,7 @@ struct Smem {
   uint32_t redu[kWarps];
   int32_t scan_tmp[kWarps];
   int32_t flag, abort, any, bt_n;
+  unsigned tctr[2];                // per-CTA tile counters of the max / expand passes
   unsigned long long prof[kProfSlots + 2];  // CTA 0's phase timers + two time marks
   int64_t bt_idx;
   int32_t bt_ok, bt_reached, bt_state, bt_pad;
@@ -485,7 +486,14 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
   const int total = S.pre_a[L];
   const LP* lpb = reinterpret_cast<const LP*>(a.lp);
   const int nw = gridDim.x * kWarps;
-  for (int tile = blockIdx.x * kWarps + warp; tile < total; tile += nw) {
+  // the CTA's tiles (b*W + j + i*nw for j < W) in order, handed to whichever
+  // of its warps is free by a shared-memory counter
+  for (;;) {
+    unsigned c_ = 0;
+    if (lane == 0) c_ = atomicAdd(&S.tctr[MODE], 1u);
+    c_ = __shfl_sync(0xffffffffu, c_, 0);
+    const int tile = blockIdx.x * kWarps + (int)(c_ % kWarps) + (int)(c_ / kWarps) * nw;
+    if (tile >= total) break;
     const int l = find_lane(S.pre_a, L, tile);
     const int k = tile - S.pre_a[l];
     const SmLane& s = S.lane[l];
@@ -527,6 +535,11 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
             sc = key_score(e.x);
             w.score[q + c + i] = sc;
             const int32_t p = c + i;
+            // a token that no other tile stages is cleared right after its
+            // read (its line is in L2 now); the first token of tile k > 0 is
+            // also staged by tile k-1 and is cleared by the expand pass
+            if (!a.lattice && p < own_hi && (p > p_lo || k == 0))
+              *ent_at(w, l, tr.state, par) = make_ulonglong2(0ull, 0ull);
             if (s.need_commit && p < own_hi) {
               // commit (§5.4): the winners-log entry {prev, arc} of the token
               const int32_t arc = key_id(e.x);
@@ -544,9 +557,9 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
             }
           } else {
             sc = __ldcg(w.score + q + c + i);
-            // the frame's entries were last read in phase X: clear this one
-            // now, while its line is likely still in L2
-            *ent_at(w, l, tr.state, par) = make_ulonglong2(0ull, 0ull);
+            // entries the max pass left (lattices, tile-boundary tokens)
+            if (a.lattice || (c + i == p_lo && k > 0))
+              *ent_at(w, l, tr.state, par) = make_ulonglong2(0ull, 0ull);
           }
           ws.off[i] = tr.off;
           ws.row[i] = tr.row;
@@ -1035,6 +1048,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
   unsigned long long steps = 0;
   unsigned long long* prof = S.prof;
   if (tid < kProfSlots) prof[tid] = 0;
+  if (tid < 2) S.tctr[tid] = 0u;
   if (tid == 0) prof[kProfSlots] = prof[kProfSlots + 1] = gtimer();
   const int tlast = 0, tsub = 1;
 
@@ -1183,6 +1197,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     prof_mark(prof, tsub, kProfPrologue);
 
     // ================= phase X: commit frame t, clear frame t-1, exact max
+    if (tid == 0) S.tctr[1] = 0u;
     if (blockIdx.x == 0) {
       for (int l = tid; l < L; l += kThreads) {
         const SmLane& s = S.lane[l];
@@ -1310,6 +1325,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     prof_mark(prof, tlast, kProfCommitMax);
 
     // ================= phase Y: expand (admit + recombine); final / partial
+    if (tid == 0) S.tctr[0] = 0u;
     for (int l = tid; l < L; l += kThreads) {
       SmLane& s = S.lane[l];
       S.pre_a[l] = 0;
@@ -1371,15 +1387,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     }
 
     {  // final step (§3) / partial (§8): one CTA per lane walks the winners log
-      if (tid == 0) {
-        int cnt = 0;
-        for (int l = 0; l < L; l++) {
-          S.pre_b[l] = cnt;
-          if (S.lane[l].phase == kFin || S.lane[l].phase == kPart) cnt++;
-        }
-        S.pre_b[L] = cnt;
-      }
+      for (int l = tid; l < L; l += kThreads)
+        S.pre_b[l] = (S.lane[l].phase == kFin || S.lane[l].phase == kPart) ? 1 : 0;
       __syncthreads();
+      lane_scan(S.pre_b, L);
       const int ntask = S.pre_b[L];
       for (int task = blockIdx.x; task < ntask; task += G) {
         const int l = find_lane(S.pre_b, L, task);
