@@ -92,6 +92,7 @@ typedef struct {
   int32_t lattice;        /* 1: persist candidates for wfst_lattice_export */
   int32_t streaming;      /* 1: decoder serves wfst_stream_* (online beam semantics) */
   int32_t options;        /* WFST_OPT_* bits, 0 = defaults */
+  int32_t gc_interval;    /* winners-log GC every gc_interval frames per lane, 0 = off (§6.3, §8.1) */
 } wfst_params;
 
 /* Turn off the per-token upper-bound skips of the max and expand passes
@@ -106,7 +107,23 @@ typedef struct {
   int64_t log_cap;        /* winners-log entries per lane (default (max_frames+2)*4*max_active, >= 1Mi) */
   int64_t lattice_cap;    /* lattice records per lane (default (max_frames+2)*2*max_active) */
   int64_t path_cap;       /* arcs of one best path (default 4*(max_frames+2)) */
+  int64_t fin_cap;        /* GC only: finalized words per lane (default 65536) */
 } wfst_capacity;
+
+/*
+ * Winners-log GC (params.gc_interval > 0; §6.3 "Winners-log GC for long-form
+ * audio", §8.1 "Per-chunk GC").  Each lane's winners log becomes a ring of
+ * log_cap entries (rounded down to a power of two, at most 2^29).  Every
+ * gc_interval frames a round finds the lane's convergence point — the newest
+ * entry that every chain from the current frontier passes through — moves
+ * the words of the path up to it (the finalized prefix) into a per-lane list
+ * of fin_cap words, cuts the chain there and frees the ring below it.  Words,
+ * scores and flags are identical to a decode without GC; a lane only needs
+ * ring space for the frames since its chains last converged, so a streaming
+ * channel can run for any length.  If the chains do not converge within the
+ * ring, the lane overflows (bit 4), as without GC.  Not with lattice = 1:
+ * lattice records refer to winners-log entries of every frame.
+ */
 
 typedef struct {
   int32_t t;          /* frame of the source node (epsilon and final records: the frame they sit in) */

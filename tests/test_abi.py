@@ -77,3 +77,27 @@ def test_graph_validation_rejects_corrupt_graphs_on_host(lib):
     h = C.c_void_p()
     assert lib.wfst_graph_upload(C.byref(desc), 0, C.byref(h)) == -2
     assert b"vocab" in lib.wfst_last_error()
+
+
+def test_binding_structs_match_the_header(tmp_path):
+    """The ctypes mirrors of wfst_params, wfst_capacity and wfst_graph_desc
+    have the header's sizes and field offsets (compiled with the host C
+    compiler against include/wfst_gb300.h)."""
+    import ctypes as C
+    structs = {"wfst_params": W.Params, "wfst_capacity": W.Capacity, "wfst_graph_desc": W.GraphDesc}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", f'#include "{HEADER}"', "int main(void) {"]
+    for cname, py in structs.items():
+        lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
+        for f, _ in py._fields_:
+            lines.append(f'  printf("{cname} {f} %zu\\n", offsetof({cname}, {f}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-o", str(exe), str(src)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    got = {tuple(l.split()[:2]): int(l.split()[2]) for l in out if l.strip()}
+    for cname, py in structs.items():
+        assert got[(cname, "size")] == C.sizeof(py), cname
+        for f, _ in py._fields_:
+            assert got[(cname, f)] == getattr(py, f).offset, (cname, f)

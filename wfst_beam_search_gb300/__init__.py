@@ -56,12 +56,12 @@ class Params(C.Structure):
     _fields_ = [("search_beam", C.c_float), ("output_beam", C.c_float),
                 ("min_active", C.c_int32), ("max_active", C.c_int32),
                 ("allow_partial", C.c_int32), ("lattice", C.c_int32), ("streaming", C.c_int32),
-                ("options", C.c_int32)]
+                ("options", C.c_int32), ("gc_interval", C.c_int32)]
 
 
 class Capacity(C.Structure):
     _fields_ = [("frontier_cap", C.c_int64), ("log_cap", C.c_int64),
-                ("lattice_cap", C.c_int64), ("path_cap", C.c_int64)]
+                ("lattice_cap", C.c_int64), ("path_cap", C.c_int64), ("fin_cap", C.c_int64)]
 
 
 _lock = threading.Lock()
@@ -271,9 +271,13 @@ MEM_NAMES = ["bytes", "frontier_cap", "log_cap", "lattice_cap", "path_cap", "gro
 
 
 def make_params(search_beam=20.0, output_beam=8.0, min_active=30, max_active=10000,
-                allow_partial=True, lattice=False, streaming=False, options=0) -> Params:
+                allow_partial=True, lattice=False, streaming=False, options=0,
+                gc_interval=0) -> Params:
+    """gc_interval > 0 turns on the winners-log GC (a GC round every
+    gc_interval frames per lane; lattice must be off)."""
     return Params(float(search_beam), float(output_beam), int(min_active), int(max_active),
-                  int(bool(allow_partial)), int(bool(lattice)), int(bool(streaming)), int(options))
+                  int(bool(allow_partial)), int(bool(lattice)), int(bool(streaming)), int(options),
+                  int(gc_interval))
 
 
 def _lp_args(lp):

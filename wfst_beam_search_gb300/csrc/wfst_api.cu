@@ -279,6 +279,17 @@ struct wfst_decoder {
   int64_t stats[WFST_STAT_COUNT] = {0};
 };
 
+// Winners-log GC: the log of a lane is a ring whose size is a power of two
+// (index & (size - 1)) of at most 2^29 entries, so that a signed chain step
+// (30 bits) and the two GC marks fit one 32-bit word.
+constexpr int64_t kMaxGcRing = (int64_t)1 << 29;
+constexpr int64_t kMaxFinCap = (int64_t)1 << 26;  // finalized words per lane
+static int64_t gc_ring_size(int64_t want) {
+  int64_t r = (int64_t)1 << 10;
+  while (r * 2 <= std::min(want, kMaxGcRing)) r *= 2;
+  return r;
+}
+
 template <typename T>
 static cudaError_t dalloc(wfst_decoder* d, T** p, size_t n, bool zero = false) {
   *p = nullptr;
@@ -338,6 +349,11 @@ extern "C" int wfst_decoder_create(wfst_graph* g, const wfst_params* params, int
   if (!(params->search_beam > 0.f) || std::isnan(params->output_beam) || params->output_beam < 0.f ||
       params->min_active < 0 || params->max_active < 0)
     return fail(WFST_ERR_INVALID_ARG, "decoder_create: beams must be positive and active bounds >= 0");
+  if (params->gc_interval < 0) return fail(WFST_ERR_INVALID_ARG, "decoder_create: gc_interval must be >= 0");
+  if (params->gc_interval > 0 && params->lattice)
+    return fail(WFST_ERR_INVALID_ARG,
+                "decoder_create: the winners-log GC needs lattice = 0 (lattice records refer to every frame's entries)");
+  const bool gc = params->gc_interval > 0;
   const DevGraph& G = g->dg;
   const int64_t N = G.N;
   int64_t qcap = (caps && caps->frontier_cap > 0) ? std::min<int64_t>(caps->frontier_cap, N) : N;
@@ -345,11 +361,17 @@ extern "C" int wfst_decoder_create(wfst_graph* g, const wfst_params* params, int
   int64_t log_cap = (caps && caps->log_cap > 0) ? caps->log_cap
                                                 : std::max<int64_t>(mf * 4 * std::max(params->max_active, 1), 1 << 20);
   log_cap = std::min<int64_t>(log_cap, (int64_t)INT32_MAX - 1);
+  if (gc) log_cap = gc_ring_size(log_cap);
+  const int64_t fin_cap = gc ? ((caps && caps->fin_cap > 0) ? std::min<int64_t>(caps->fin_cap, kMaxFinCap) : 65536) : 0;
   int64_t lat_cap = 0;
   if (params->lattice)
     lat_cap = (caps && caps->lattice_cap > 0) ? caps->lattice_cap
                                               : std::max<int64_t>(mf * 2 * std::max(params->max_active, 1), 1 << 20);
-  int64_t path_cap = (caps && caps->path_cap > 0) ? caps->path_cap : 4 * mf * (1 + (int64_t)G.eps_depth);
+  // with the GC a backtrack walks only back to the last cut, which can lag
+  // the frontier by more than a chunk: room for 4096 frames of arcs
+  int64_t path_cap = (caps && caps->path_cap > 0)
+                         ? caps->path_cap
+                         : 4 * std::max<int64_t>(mf, gc ? 1024 : 0) * (1 + (int64_t)G.eps_depth);
   path_cap = std::min<int64_t>(path_cap, (int64_t)INT32_MAX / 2);
   if (qcap > (int64_t)INT32_MAX || lat_cap > ((int64_t)1 << 40))
     return fail(WFST_ERR_CAPACITY, "decoder_create: capacities exceed the 32-bit tables");
@@ -366,6 +388,8 @@ extern "C" int wfst_decoder_create(wfst_graph* g, const wfst_params* params, int
   w.N = (int32_t)N;
   w.qcap = qcap;
   w.log_cap = log_cap;
+  w.log_mask = gc ? (unsigned long long)(log_cap - 1) : ~0ull;
+  w.fin_cap = fin_cap;
   w.lat_cap = lat_cap;
   w.path_cap = path_cap;
   w.tiles_cap = G.A / kTile + 2;
@@ -388,6 +412,7 @@ extern "C" int wfst_decoder_create(wfst_graph* g, const wfst_params* params, int
   }
   DA(w.wl_cnt, 3 * L, true);
   DA(w.wlog, L * log_cap, false);
+  if (gc) DA(w.fin, L * fin_cap, false);
   DA(w.fcnt, 4 * L, true);
   DA(w.lanes, L, true);
   DA(w.stats, L, true);
@@ -532,6 +557,7 @@ static int run_call(wfst_decoder* d, const void* lp, int32_t dtype, int64_t stri
   a.lattice = d->p.lattice;
   a.nblocks = d->grid[dtype == WFST_F16 ? 1 : 0];
   a.ub_skip = (d->p.options & WFST_OPT_NO_UB_SKIP) ? 0 : 1;
+  a.gc_interval = d->p.gc_interval;
   CU(cudaEventRecord(d->ev0, st), "event");
   CU(launch_decode(a, dtype, a.nblocks, st), "decode kernel launch");
   CU(cudaEventRecord(d->ev1, st), "event");
@@ -632,12 +658,14 @@ static int grow_capacities(wfst_decoder* d, bool g_log, bool g_lat, bool g_q, bo
   const size_t L = (size_t)d->L;
   const DevGraph& G = d->g->dg;
   struct Plan { void** slot; size_t bytes; void* fresh; };
-  Plan plan[8];
+  Plan plan[10];
   int np = 0;
-  int64_t log_cap = w.log_cap, lat_cap = w.lat_cap, qcap = w.qcap, path_cap = w.path_cap;
+  int64_t log_cap = w.log_cap, lat_cap = w.lat_cap, qcap = w.qcap, path_cap = w.path_cap, fin_cap = w.fin_cap;
   const int64_t path_bound = 2 * ((int64_t)d->max_frames + 2) * (1 + (int64_t)G.eps_depth);
-  if (g_log && w.log_cap < (int64_t)INT32_MAX - 1) {
-    log_cap = std::min<int64_t>(2 * w.log_cap, (int64_t)INT32_MAX - 1);
+  const bool gc = d->p.gc_interval > 0;
+  const int64_t log_bound = gc ? kMaxGcRing : (int64_t)INT32_MAX - 1;
+  if (g_log && w.log_cap < log_bound) {
+    log_cap = std::min<int64_t>(2 * w.log_cap, log_bound);
     plan[np++] = {(void**)&w.wlog, sizeof(int2) * L * (size_t)log_cap, nullptr};
     if (w.lattice) plan[np++] = {(void**)&w.bwd, sizeof(uint32_t) * L * (size_t)log_cap, nullptr};
   }
@@ -656,6 +684,10 @@ static int grow_capacities(wfst_decoder* d, bool g_log, bool g_lat, bool g_q, bo
     path_cap = std::min<int64_t>(2 * w.path_cap, path_bound);
     plan[np++] = {(void**)&w.path, sizeof(int32_t) * L * (size_t)path_cap, nullptr};
   }
+  if (g_path && gc && w.fin_cap < kMaxFinCap) {  // the finalized-word list shares the path bit
+    fin_cap = std::min<int64_t>(2 * w.fin_cap, kMaxFinCap);
+    plan[np++] = {(void**)&w.fin, sizeof(int32_t) * L * (size_t)fin_cap, nullptr};
+  }
   if (np == 0) return fail(WFST_ERR_CAPACITY, "decode: capacities are at their bounds");
   for (int i = 0; i < np; i++) {
     if (cudaMalloc(&plan[i].fresh, plan[i].bytes) != cudaSuccess) {
@@ -666,6 +698,8 @@ static int grow_capacities(wfst_decoder* d, bool g_log, bool g_lat, bool g_q, bo
   }
   for (int i = 0; i < np; i++) dswap(d, plan[i].slot, plan[i].fresh, plan[i].bytes);
   w.log_cap = log_cap;
+  if (gc) w.log_mask = (unsigned long long)(log_cap - 1);
+  w.fin_cap = fin_cap;
   w.lat_cap = lat_cap;
   w.qcap = qcap;
   w.path_cap = path_cap;

@@ -70,6 +70,9 @@ struct LaneState {                // persistent per lane (mirrored in shared mem
   int32_t t_eff;                  // offline length (last-frames rule), -1 streaming
   int32_t bt_top;                 // frame of the last backtracked path's newest token, -1 = none
   int32_t bt_len;                 // arcs of that path (kept oldest-first in path)
+  int32_t gc_t;                   // frames consumed at the lane's last winners-log GC round
+  int64_t floor;                  // winners-log GC root: entries below it are free (0 without GC)
+  int32_t fin_n;                  // finalized words (the GC-cut prefix of the best path)
   int32_t pad;
 };
 
@@ -136,7 +139,11 @@ struct DevWork {
   float* maxlp;                   // [L][max_frames] max log-prob of each row of the call
   uint32_t* mark;                 // [L][N] worklist dedupe marks
   unsigned long long* wl_cnt;     // [3][L] (tokens << 32) | epsilon arcs
-  int2* wlog;                     // [L][log_cap] {prev, arc} winners log
+  int2* wlog;                     // [L][log_cap] winners log {delta, arc}: the predecessor is
+                                  // entry i - delta (0 = none); a ring (index & log_mask) with GC
+  unsigned long long log_mask;    // log_cap - 1 with GC (log_cap a power of two), else all ones
+  int32_t* fin;                   // [L][fin_cap] finalized words (GC)
+  int64_t fin_cap;
   FrameCnt* fcnt;                 // [4][L]
   LaneState* lanes;               // [L]
   LaneStats* stats;               // [L]
@@ -171,6 +178,7 @@ struct RunArgs {
   int32_t min_active, max_active, allow_partial, lattice;
   int32_t nblocks;
   int32_t ub_skip;                // upper-bound skips in the max/expand passes
+  int32_t gc_interval;            // winners-log GC every gc_interval frames, 0 = off
 };
 
 }  // namespace wfst

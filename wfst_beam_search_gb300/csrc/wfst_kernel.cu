@@ -54,6 +54,10 @@ struct SmLane {
   float cur_max;                  // this step's exact max end (expand pass)
   int32_t seed_next;              // the expand pass seeds the next step's max
   int32_t prev_cleared;           // the previous frame's entries were cleared by its expand pass
+  int64_t floor;                  // winners-log GC root (entries below it are free)
+  int32_t fin_n;                  // finalized words of the lane (GC)
+  int32_t gc_t;                   // frames consumed at the last GC round
+  int32_t gc_due;                 // a GC round runs at the end of this step
 };
 
 struct WStage {                   // one warp's staged tokens of its current tile
@@ -87,6 +91,8 @@ struct Smem {
   int32_t bt_ok, bt_reached, bt_state, bt_pad;
   int32_t bt_d, bt_lo, bt_hi;
   float bt_score;
+  unsigned long long gc_min;      // GC round: deepest anchor-chain depth another chain met
+  int32_t gc_ok, gc_nw;
 };
 
 // ------------------------------------------------------------------ helpers
@@ -353,6 +359,35 @@ __device__ __forceinline__ int relax_ent(const RunArgs& a, ulonglong2* e, unsign
 }
 
 __device__ __forceinline__ uint32_t ent_src(const ulonglong2& e) { return (uint32_t)e.y; }
+
+// Winners-log entry i (a logical index) of lane l: {delta, arc}, the
+// predecessor being entry i - delta (delta 0: none; arc -1: the start token
+// or a GC root).  delta is signed: an epsilon arc's source token sits in the
+// same frame, possibly at a later position.  Without the GC, delta is the
+// whole 32-bit word and the log is flat.  With the GC the log is a ring
+// (i & log_mask), delta is the low 30 bits (two's complement) and a GC round
+// marks entries with the two high bits; an anchor-chain entry holds its
+// depth on the chain in the low bits while it is marked.
+constexpr uint32_t kMarkAnchor = 0x80000000u;  // on the anchor chain of a GC round
+constexpr uint32_t kMarkWalk = 0x40000000u;    // on another token's walk of a GC round
+constexpr uint32_t kDeltaMask = 0x3fffffffu;
+__device__ __forceinline__ int32_t sext30(uint32_t x) { return (int32_t)(x << 2) >> 2; }
+__device__ __forceinline__ int32_t wlog_delta(const RunArgs& a, int32_t x) {
+  return a.gc_interval > 0 ? sext30((uint32_t)x) : x;
+}
+__device__ __forceinline__ int2* wlog_at(const DevWork& w, int l, int64_t i) {
+  return w.wlog + (size_t)l * (size_t)w.log_cap + (size_t)((unsigned long long)i & w.log_mask);
+}
+// The winners-log entry of a frame token: its arc and the distance back to
+// the token it came from (0 for the start token).
+__device__ __forceinline__ void wlog_commit(const RunArgs& a, int l, int64_t idx, int64_t floor,
+                                            int32_t arc, int64_t prev) {
+  const DevWork& w = a.w;
+  const int64_t d = arc < 0 ? 0 : idx - prev;
+  const int32_t x = a.gc_interval > 0 ? (int32_t)((uint32_t)d & kDeltaMask) : (int32_t)d;
+  if (idx - floor < w.log_cap) *wlog_at(w, l, idx) = make_int2(x, arc);
+  else lane_ovf(a, l, kOvfArena);
+}
 // Token positions per state are kept only where something looks a state's
 // token up (epsilon worklists, lattice records); the final backtrack of other
 // graphs finds its one token by a scan of the frame.
@@ -545,11 +580,8 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
               const int32_t arc = key_id(e.x);
               const uint32_t src = ent_src(e);
               const int64_t base_new = s.cursor, base_old = s.base_cur;
-              const int32_t prev =
-                  arc < 0 ? -1 : (int32_t)(((src >> 31) ? base_new : base_old) + (src & 0x7fffffffu));
-              const int64_t idx = base_new + p;
-              if (idx < w.log_cap) w.wlog[(size_t)l * w.log_cap + idx] = make_int2(prev, arc);
-              else lane_ovf(a, l, kOvfArena);
+              const int64_t prev = ((src >> 31) ? base_new : base_old) + (src & 0x7fffffffu);
+              wlog_commit(a, l, base_new + p, s.floor, arc, prev);
               if (g.has_eps) {
                 const int4 m = __ldg(g.meta + tr.state);
                 if (m.z > m.y) atomicAdd(&w.stats[l].eps, (unsigned long long)(m.z - m.y));
@@ -838,6 +870,139 @@ __device__ bool run_closure(const RunArgs& a, Smem& S, unsigned& epoch) {
   return true;
 }
 
+// ------------------------------------------------------------------ winners-log GC
+
+// One winners-log GC round of lane l (§6.3 "Winners-log GC", §8.1 "Per-chunk
+// GC"), run by one CTA at the end of a step.  Frame t's tokens are the
+// entries [base_cur, cursor) and every live chain passes through one of them.
+//   1. thread 0 marks the first token's chain (the anchor chain) back to the
+//      root, writing each entry's depth on the chain into it and keeping its
+//      delta in the lane's path buffer (free here: the next backtrack walks
+//      the whole tail again);
+//   2. every other token walks its own chain, marking it, until it meets a
+//      marked entry; meeting the anchor chain posts that entry's depth.  The
+//      deepest such entry E is on every chain: each chain joins the anchor
+//      chain at or above E and follows it from there (a chain that meets
+//      another walk follows that walk to its meeting point);
+//   3. the marks are cleared and the anchor chain's deltas restored;
+//   4. the words of the path from the root up to E are appended to the
+//      lane's finalized words, E becomes the root (arc -1, no predecessor)
+//      and the ring below it is free.
+// Depth, not index, orders the meeting points: an epsilon arc's source token
+// can sit at a later position of the same frame.  Lanes whose log, frontier
+// or path overflowed are left alone.
+__device__ void gc_round(const RunArgs& a, Smem& S, int l) {
+  const DevWork& w = a.w;
+  const DevGraph& g = a.g;
+  const SmLane& s = S.lane[l];
+  const int tid = threadIdx.x;
+  const int64_t lo = s.base_cur, hi = s.cursor, root = s.floor;
+  const int64_t max_hops = hi - root;
+  int32_t* keep = w.path + (size_t)l * (size_t)w.path_cap;  // anchor-chain deltas by depth
+  if (tid == 0) {
+    S.gc_min = 0;   // deepest meeting depth (the anchor itself: 0)
+    S.gc_nw = 0;    // anchor-chain entries marked
+    S.gc_ok = ((__ldcg(&w.lanes[l].overflow) & (kOvfArena | kOvfKept | kOvfPath)) == 0 && root <= lo &&
+               lo < hi && hi - root <= w.log_cap) ? 1 : 0;
+    if (S.gc_ok) {
+      int64_t i = lo;
+      for (int32_t dep = 0;; dep++) {
+        if (i < root || i >= hi || dep >= w.path_cap || dep > max_hops) { S.gc_ok = 0; break; }
+        int2* p = wlog_at(w, l, i);
+        const int2 e = __ldcg(p);
+        keep[dep] = e.x;
+        p->x = (int32_t)(kMarkAnchor | (uint32_t)dep);
+        S.gc_nw = dep + 1;
+        if (e.y < 0) break;  // the root
+        const int32_t dl = sext30((uint32_t)e.x);
+        if (dl == 0) { S.gc_ok = 0; break; }
+        i -= dl;
+      }
+    }
+  }
+  __threadfence();  // marks reach L2 before the walks read them
+  __syncthreads();
+  const bool run = S.gc_ok != 0;
+  if (run) {
+    for (int64_t x = lo + 1 + tid; x < hi; x += kThreads) {
+      int64_t i = x;
+      for (int64_t h = 0; h <= max_hops && i >= root && i < hi; h++) {
+        int2* p = wlog_at(w, l, i);
+        const int2 e = __ldcg(p);
+        const uint32_t dx = (uint32_t)e.x;
+        if (dx & kMarkAnchor) { atomicMax(&S.gc_min, (unsigned long long)(dx & kDeltaMask)); break; }
+        if (dx & kMarkWalk) break;  // another walk continues from here
+        p->x = (int32_t)(dx | kMarkWalk);
+        const int32_t dl = sext30(dx);
+        if (e.y < 0 || dl == 0) break;  // (an unmarked root cannot occur)
+        i -= dl;
+      }
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (run) {  // clear the walks' marks (each walk ends where its own marks end)
+    for (int64_t x = lo + 1 + tid; x < hi; x += kThreads) {
+      int64_t i = x;
+      for (int64_t h = 0; h <= max_hops && i >= root && i < hi; h++) {
+        int2* p = wlog_at(w, l, i);
+        const uint32_t dx = (uint32_t)__ldcg(&p->x);
+        if (!(dx & kMarkWalk)) break;
+        const uint32_t cx = dx & ~kMarkWalk;
+        p->x = (int32_t)cx;
+        const int32_t dl = sext30(cx);
+        if (dl == 0) break;
+        i -= dl;
+      }
+    }
+  }
+  if (tid == 0) {  // restore the anchor chain; E = its entry at the deepest meeting depth
+    int64_t i = lo, E = -1;
+    for (int32_t dep = 0; dep < S.gc_nw; dep++) {
+      const int32_t x = keep[dep];
+      wlog_at(w, l, i)->x = x;
+      if ((unsigned long long)dep == S.gc_min) E = i;
+      i -= sext30((uint32_t)x);
+    }
+    S.bt_idx = E;
+    w.lanes[l].bt_top = -1;  // the path buffer was scratch space
+    w.lanes[l].bt_len = 0;
+  }
+  __threadfence();
+  __syncthreads();
+  // cut at E: the words from the root up to E are final
+  if (tid == 0 && run && S.gc_min + 1 < (unsigned long long)S.gc_nw && S.bt_idx >= 0) {
+    const int64_t E = S.bt_idx;
+    const int32_t hops = (int32_t)(S.gc_nw - 1 - (int32_t)S.gc_min);  // arcs from E down to the root
+    int32_t nw = 0;
+    int64_t i = E;
+    for (int32_t h = 0; h < hops; h++) {
+      const int2 e = __ldcg(wlog_at(w, l, i));
+      if (e.y < 0) break;
+      if (__ldg(g.c_olabel + e.y) != 0) nw++;
+      i -= sext30((uint32_t)e.x);
+    }
+    if ((int64_t)s.fin_n + nw > w.fin_cap) {
+      lane_ovf(a, l, kOvfPath);  // no room for the finalized words: no cut
+    } else {
+      int32_t* fin = w.fin + (size_t)l * (size_t)w.fin_cap;
+      int32_t k = s.fin_n + nw;
+      i = E;
+      for (int32_t h = 0; h < hops; h++) {
+        const int2 e = __ldcg(wlog_at(w, l, i));
+        if (e.y < 0) break;
+        const int32_t o = __ldg(g.c_olabel + e.y);
+        if (o != 0 && k > s.fin_n) fin[--k] = o;
+        i -= sext30((uint32_t)e.x);
+      }
+      *wlog_at(w, l, E) = make_int2(0, -1);
+      w.lanes[l].floor = E;
+      w.lanes[l].fin_n = s.fin_n + nw;
+    }
+  }
+  __syncthreads();
+}
+
 // ------------------------------------------------------------------ lane setup
 
 __device__ void init_lane_global(const RunArgs& a, int l) {
@@ -854,6 +1019,8 @@ __device__ void init_lane_global(const RunArgs& a, int l) {
   w.lanes[l].overflow = 0;
   w.lanes[l].bt_top = -1;  // no path to continue from
   w.lanes[l].bt_len = 0;
+  w.lanes[l].floor = 0;
+  w.lanes[l].fin_n = 0;
   const int32_t s0 = g.start;
   const int4 m = __ldg(g.meta + s0);
   const uint32_t deg = (uint32_t)(m.y - m.x);
@@ -1066,6 +1233,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     s.base_prev = st.base_prev;
     s.eps_pass = st.eps_pass;
     s.t_eff = st.t_eff;
+    s.floor = st.floor;
+    s.fin_n = st.fin_n;
+    s.gc_t = st.gc_t;
+    s.gc_due = 0;
     s.row = c.row;
     s.flags = c.row >= 0 ? c.flags : 0;
     s.phase = kNone;
@@ -1085,6 +1256,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
       s.beam = a.search_beam;
       s.cursor = s.base_cur = s.base_prev = 0;
       s.t_eff = c.t_eff;
+      s.floor = 0;
+      s.fin_n = 0;
+      s.gc_t = 0;
     }
     s.t0 = s.t;
     s.t_end = s.t + (c.row >= 0 ? c.nframes : 0);
@@ -1135,6 +1309,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
       if (s.row < 0 || s.status != kLaneRunning) continue;
       if (s.was_emit) s.sum_m += __ldcg(&fc_of(w, s.t, l)->cnt) >> 32;
       s.was_emit = 0;
+      if (s.gc_due) {  // a GC round of the last step moved the root and finalized words
+        s.floor = __ldcg(&w.lanes[l].floor);
+        s.fin_n = __ldcg(&w.lanes[l].fin_n);
+        s.gc_due = 0;
+      }
       if (s.t < s.t_end) s.phase = kEmit;
       else if ((s.flags & kCallFinal) && !s.done_final) s.phase = kFin;
       else if ((s.flags & kCallPartial) && !(s.flags & kCallFinal) && !s.done_partial) s.phase = kPart;
@@ -1253,11 +1432,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
             const int64_t base_new = s.cursor;   // frame f
             const int64_t base_old = s.base_cur; // frame f-1
             // the winner's source token: same frame for an epsilon arc, else the previous one
-            const int32_t prev =
-                arc < 0 ? -1 : (int32_t)(((src[k] >> 31) ? base_new : base_old) + (src[k] & 0x7fffffffu));
-            const int64_t idx = base_new + pk[k];
-            if (idx < w.log_cap) w.wlog[(size_t)l * w.log_cap + idx] = make_int2(prev, arc);
-            else lane_ovf(a, l, kOvfArena);
+            const int64_t prev = ((src[k] >> 31) ? base_new : base_old) + (src[k] & 0x7fffffffu);
+            wlog_commit(a, l, base_new + pk[k], s.floor, arc, prev);
             if (g.has_eps) {
               const int4 m = __ldg(g.meta + st[k]);
               if (m.z > m.y) atomicAdd(&w.stats[l].eps, (unsigned long long)(m.z - m.y));
@@ -1337,6 +1513,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         s.committed = s.t;
       }
       s.expanded = 0;
+      // winners-log GC of frame t (committed above) at the end of this step
+      s.gc_due = (a.gc_interval > 0 && s.phase == kEmit && s.n_cur > 0 && s.t + 1 - s.gc_t >= a.gc_interval)
+                     ? 1 : 0;
+      if (s.gc_due) s.gc_t = s.t + 1;
       if (s.phase == kEmit) {
         const unsigned mk = __ldcg(&fc_of(w, s.t, l)->maxkey);
         s.expanded = mk != 0u;
@@ -1388,7 +1568,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
 
     {  // final step (§3) / partial (§8): one CTA per lane walks the winners log
       for (int l = tid; l < L; l += kThreads)
-        S.pre_b[l] = (S.lane[l].phase == kFin || S.lane[l].phase == kPart) ? 1 : 0;
+        S.pre_b[l] = (S.lane[l].phase == kFin || S.lane[l].phase == kPart || S.lane[l].gc_due) ? 1 : 0;
       __syncthreads();
       lane_scan(S.pre_b, L);
       const int ntask = S.pre_b[L];
@@ -1396,6 +1576,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         const int l = find_lane(S.pre_b, L, task);
         const SmLane& s = S.lane[l];
         const int f = s.t, par = f & 1;
+        if (s.gc_due) {
+          gc_round(a, S, l);
+          continue;
+        }
         if (tid == 0) {
           const FrameCnt* fc = fc_of(w, f, l);
           const unsigned long long fk = __ldcg(&fc->final_key);
@@ -1443,13 +1627,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
           int64_t n = 0;
           int32_t* path = w.path + (size_t)l * w.path_cap;
           int2* pf = w.pframe + (size_t)l * (w.max_frames + 2);
-          const int2* lg = w.wlog + (size_t)l * w.log_cap;
           const int prev_top = __ldcg(&w.lanes[l].bt_top);
           int32_t d = -1;  // path position of the meeting entry (-1: the walk reached the start)
           int32_t fr = f, fr_seen = f + 1;
           int64_t i = idx;
-          const int64_t limit = min(s.cursor, w.log_cap);
-          while (ok && i >= 0 && i < limit && n <= limit) {
+          // entries [floor, cursor) are live (floor: the GC root, else 0)
+          const int64_t lo_i = s.floor, hi_i = s.cursor;
+          while (ok && i >= lo_i && i < hi_i && i - lo_i < w.log_cap && n <= hi_i - lo_i) {
             // (frames past the table, possible on a long stream, are simply
             // not recorded: the walk meets the earlier path at a later check)
             if (fr != fr_seen) {  // the first entry of frame fr on this walk
@@ -1461,12 +1645,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
               if (in_table) pf[fr] = make_int2((int32_t)i, (int32_t)n);
               fr_seen = fr;
             }
-            const int2 e = __ldcg(lg + i);
+            const int2 e = __ldcg(wlog_at(w, l, i));
             if (e.y < 0) break;
             if (n < w.path_cap) path[w.path_cap - 1 - n] = e.y;
             n++;
             if (!(__ldg(g.c_src + e.y) >> 31)) fr--;  // an emitting arc ends one frame later
-            i = e.x;
+            const int32_t dl = wlog_delta(a, e.x);
+            if (dl == 0) break;
+            i -= dl;
           }
           const int64_t len = (int64_t)d + 1 + n;
           if (n > w.path_cap || len + n > w.path_cap) {
@@ -1518,11 +1704,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
           }
           __syncthreads();
         }
-        // words = the path's non-zero output labels, forward order
+        // words = the finalized words (GC), then the path's non-zero output
+        // labels, forward order
         const int n = S.bt_n;
         const int32_t* path = w.path + (size_t)l * w.path_cap;
         int32_t* out = w.words + (size_t)l * a.words_cap;
-        int run = 0;
+        const int nfin = S.bt_ok ? s.fin_n : 0;
+        for (int j = tid; j < min(nfin, a.words_cap); j += kThreads)
+          out[j] = __ldcg(w.fin + (size_t)l * (size_t)w.fin_cap + j);
+        int run = nfin;
         for (int base = 0; base < n; base += kThreads) {
           const int j = base + tid;
           int32_t o = 0;
@@ -1641,6 +1831,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
       st.base_prev = s.base_prev;
       st.eps_pass = s.eps_pass;
       st.t_eff = s.t_eff;
+      st.gc_t = s.gc_t;
       LaneStats& ls = w.stats[l];
       ls.frames += s.frames;
       ls.sum_n += s.sum_n;

@@ -123,6 +123,7 @@ size_t layout(unsigned char* base, const DevGraph& G, int L, int T, const wfst_p
   const int64_t log_bound = mf * w.qcap;
   const int64_t log_default = std::max<int64_t>(mf * 4 * std::max(p.max_active, 1), 1 << 20);
   w.log_cap = std::min(log_bound, log_default);
+  w.log_mask = ~0ull;  // a flat log (no winners-log GC here)
   w.lat_cap = 0;
   w.path_cap = 4 * mf * (1 + (int64_t)G.eps_depth);
   w.tiles_cap = G.A / kTile + 2;
@@ -201,8 +202,8 @@ extern "C" int wfst_decode_static(const wfst_graph* g, const wfst_params* params
                                   int32_t B, int32_t T, void* stream, int32_t* words, int32_t words_cap,
                                   int32_t* word_lens, double* scores, int32_t* meta) {
   if (!g || !params) return api_fail(WFST_ERR_INVALID_ARG, "decode_static: NULL graph or params");
-  if (params->lattice || params->streaming)
-    return api_fail(WFST_ERR_INVALID_ARG, "decode_static: lattice and streaming must be 0");
+  if (params->lattice || params->streaming || params->gc_interval)
+    return api_fail(WFST_ERR_INVALID_ARG, "decode_static: lattice, streaming and gc_interval must be 0");
   if (!(params->search_beam > 0.f) || std::isnan(params->output_beam) || params->output_beam < 0.f ||
       params->min_active < 0 || params->max_active < 0)
     return api_fail(WFST_ERR_INVALID_ARG, "decode_static: beams must be positive and active bounds >= 0");
