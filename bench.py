@@ -228,8 +228,9 @@ def run_gpu(args):
     g = synth.make_graph(args.workload)
     G = W.Graph(g, device=local)
     params = W.make_params(wl.search_beam, wl.output_beam, wl.min_active, wl.max_active, True,
-                           wl.lattice and wl.streaming, streaming=wl.streaming,
-                           options=W.OPT_NO_UB_SKIP if args.no_ub_skip else 0)
+                           wl.lattice and wl.streaming and not args.gc_interval, streaming=wl.streaming,
+                           options=W.OPT_NO_UB_SKIP if args.no_ub_skip else 0,
+                           gc_interval=args.gc_interval)
     nl = args.lanes or wl.B
     caps = W.Capacity(args.frontier_cap, args.log_cap, 0, 0) if (args.log_cap or args.frontier_cap) else None
     D = W.Decoder(G, params, nl, wl.T, caps)
@@ -340,7 +341,8 @@ def run_gpu(args):
                    "min_active": wl.min_active, "parallelism": f"replicas x{ws} (lanes sharded)",
                    "l2": "inputs larger than L2 (320 MB log-probs, 218 MB graph); no flush",
                    "mode": (f"streaming: {wl.chunk}-frame chunks, partial per chunk, finalize with lattice"
-                            if wl.streaming else "offline")},
+                            if wl.streaming else "offline"),
+                   "gc_interval": args.gc_interval},
         "arcs_expanded_per_s": arcs_per_s,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": measured_traffic(workload_name(wl), B),
@@ -378,6 +380,8 @@ def main():
     ap.add_argument("--no-ub-skip", action="store_true", help="turn off the exact upper-bound skips")
     ap.add_argument("--frontier-cap", type=int, default=0, help="tokens per lane per frame (0: default)")
     ap.add_argument("--log-cap", type=int, default=0, help="winners-log entries per lane (0: default)")
+    ap.add_argument("--gc-interval", type=int, default=0,
+                    help="winners-log GC every N frames per lane (0: off; turns the lattice off)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

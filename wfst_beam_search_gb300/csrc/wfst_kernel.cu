@@ -889,8 +889,10 @@ __device__ bool run_closure(const RunArgs& a, Smem& S, unsigned& epoch) {
 //      lane's finalized words, E becomes the root (arc -1, no predecessor)
 //      and the ring below it is free.
 // Depth, not index, orders the meeting points: an epsilon arc's source token
-// can sit at a later position of the same frame.  Lanes whose log, frontier
-// or path overflowed are left alone.
+// can sit at a later position of the same frame.  Walks are capped at H hops
+// (a few GC intervals of frames): if some chain has not met the anchor chain
+// within H hops the chains have not converged yet and the round cuts nothing.
+// Lanes whose log, frontier or path overflowed are left alone.
 __device__ void gc_round(const RunArgs& a, Smem& S, int l) {
   const DevWork& w = a.w;
   const DevGraph& g = a.g;
@@ -898,6 +900,8 @@ __device__ void gc_round(const RunArgs& a, Smem& S, int l) {
   const int tid = threadIdx.x;
   const int64_t lo = s.base_cur, hi = s.cursor, root = s.floor;
   const int64_t max_hops = hi - root;
+  const int64_t H = min((int64_t)w.path_cap - 1,
+                        (int64_t)(4 * a.gc_interval + 64) * (1 + (int64_t)g.eps_depth));
   int32_t* keep = w.path + (size_t)l * (size_t)w.path_cap;  // anchor-chain deltas by depth
   if (tid == 0) {
     S.gc_min = 0;   // deepest meeting depth (the anchor itself: 0)
@@ -906,8 +910,8 @@ __device__ void gc_round(const RunArgs& a, Smem& S, int l) {
                lo < hi && hi - root <= w.log_cap) ? 1 : 0;
     if (S.gc_ok) {
       int64_t i = lo;
-      for (int32_t dep = 0;; dep++) {
-        if (i < root || i >= hi || dep >= w.path_cap || dep > max_hops) { S.gc_ok = 0; break; }
+      for (int32_t dep = 0; dep <= H; dep++) {
+        if (i < root || i >= hi || dep > max_hops) { S.gc_ok = 0; break; }
         int2* p = wlog_at(w, l, i);
         const int2 e = __ldcg(p);
         keep[dep] = e.x;
@@ -926,17 +930,26 @@ __device__ void gc_round(const RunArgs& a, Smem& S, int l) {
   if (run) {
     for (int64_t x = lo + 1 + tid; x < hi; x += kThreads) {
       int64_t i = x;
-      for (int64_t h = 0; h <= max_hops && i >= root && i < hi; h++) {
+      bool met = false;
+      for (int64_t h = 0; h <= H && i >= root && i < hi; h++) {
         int2* p = wlog_at(w, l, i);
         const int2 e = __ldcg(p);
         const uint32_t dx = (uint32_t)e.x;
-        if (dx & kMarkAnchor) { atomicMax(&S.gc_min, (unsigned long long)(dx & kDeltaMask)); break; }
-        if (dx & kMarkWalk) break;  // another walk continues from here
+        if (dx & kMarkAnchor) {
+          atomicMax(&S.gc_min, (unsigned long long)(dx & kDeltaMask));
+          met = true;
+          break;
+        }
+        if (dx & kMarkWalk) {  // another walk continues from here
+          met = true;
+          break;
+        }
         p->x = (int32_t)(dx | kMarkWalk);
         const int32_t dl = sext30(dx);
         if (e.y < 0 || dl == 0) break;  // (an unmarked root cannot occur)
         i -= dl;
       }
+      if (!met) S.gc_ok = 0;  // not converged within H hops: no cut this round
     }
   }
   __threadfence();
@@ -944,7 +957,7 @@ __device__ void gc_round(const RunArgs& a, Smem& S, int l) {
   if (run) {  // clear the walks' marks (each walk ends where its own marks end)
     for (int64_t x = lo + 1 + tid; x < hi; x += kThreads) {
       int64_t i = x;
-      for (int64_t h = 0; h <= max_hops && i >= root && i < hi; h++) {
+      for (int64_t h = 0; h <= H && i >= root && i < hi; h++) {
         int2* p = wlog_at(w, l, i);
         const uint32_t dx = (uint32_t)__ldcg(&p->x);
         if (!(dx & kMarkWalk)) break;
@@ -971,12 +984,11 @@ __device__ void gc_round(const RunArgs& a, Smem& S, int l) {
   __threadfence();
   __syncthreads();
   // cut at E: the words from the root up to E are final
-  if (tid == 0 && run && S.gc_min + 1 < (unsigned long long)S.gc_nw && S.bt_idx >= 0) {
+  if (tid == 0 && run && S.gc_ok && S.bt_idx > root) {
     const int64_t E = S.bt_idx;
-    const int32_t hops = (int32_t)(S.gc_nw - 1 - (int32_t)S.gc_min);  // arcs from E down to the root
     int32_t nw = 0;
     int64_t i = E;
-    for (int32_t h = 0; h < hops; h++) {
+    for (int64_t h = 0; h <= max_hops && i >= root && i < hi; h++) {
       const int2 e = __ldcg(wlog_at(w, l, i));
       if (e.y < 0) break;
       if (__ldg(g.c_olabel + e.y) != 0) nw++;
@@ -988,7 +1000,7 @@ __device__ void gc_round(const RunArgs& a, Smem& S, int l) {
       int32_t* fin = w.fin + (size_t)l * (size_t)w.fin_cap;
       int32_t k = s.fin_n + nw;
       i = E;
-      for (int32_t h = 0; h < hops; h++) {
+      for (int64_t h = 0; h <= max_hops && i >= root && i < hi; h++) {
         const int2 e = __ldcg(wlog_at(w, l, i));
         if (e.y < 0) break;
         const int32_t o = __ldg(g.c_olabel + e.y);
