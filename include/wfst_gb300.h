@@ -300,6 +300,28 @@ int wfst_decode_static(const wfst_graph* g, const wfst_params* params, const voi
                        int32_t B, int32_t T, void* stream, int32_t* words, int32_t words_cap,
                        int32_t* word_lens, double* scores, int32_t* meta);
 
+/*
+ * Blank-skip frame pre-slicing, a pre-pass outside the decoder (§3 Decoding
+ * Semantics: "blank-skip stays outside the decoder", WeNet-style, threshold
+ * 0.98 by default).  Frame t < lens[b] of lane b is dropped iff
+ * log_probs[b, t, blank_id] > log(threshold), with log(threshold) computed in
+ * double and rounded once to fp32 and the log-prob widened exactly to fp32.
+ * The kept rows are packed in order into out[b, i, v] at out + (b*T + i)*V
+ * (same dtype), out_lens[b] receives the kept count and frame_map[b*T + i] the
+ * source frame of kept row i (-1 past the count).  Decode the result with
+ * lens = out_lens and stride_t = V, stride_b = T*V.
+ * log_probs [B, T, V] with strides as in wfst_decode; lens, out, out_lens and
+ * frame_map are DEVICE arrays ([B], [B*T*V], [B], [B*T]); nothing is
+ * allocated and nothing is copied to the host: the two kernels are enqueued on
+ * `stream` and the call returns without waiting.  Rows past out_lens[b] are
+ * left as they were.  Errors: INVALID_ARG (NULL or host pointers, blank_id out
+ * of [0, V), threshold <= 0, bad strides), CUDA.
+ */
+int wfst_blank_skip(const void* log_probs, int32_t dtype, int64_t stride_b, int64_t stride_t,
+                    int32_t vocab_size, int32_t blank_id, float threshold, const int32_t* lens,
+                    int32_t B, int32_t T, void* out, int32_t* out_lens, int32_t* frame_map,
+                    void* stream);
+
 const char* wfst_last_error(void);
 
 #ifdef __cplusplus

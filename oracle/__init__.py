@@ -236,3 +236,26 @@ def decode_batch(graph: Graph, lp, lens, p: dict, threads: int = 1, lattice_out=
     with ThreadPoolExecutor(max_workers=threads) as ex:
         futs = [ex.submit(decode, graph, lp[b], lens[b], p, lattice_out) for b in range(len(lens))]
         return [f.result() for f in futs]
+
+
+def blank_skip(lp, lens, threshold=0.98, blank=0):
+    """Blank-skip frame pre-slicing, outside the decoder (page "GPU WFST
+    Beam-Search Decoder", §3 Decoding Semantics: blank-skip stays outside the
+    decoder, WeNet-style frame pre-slicing, threshold 0.98 by default).
+
+    Frame t < lens[b] of lane b is dropped when its blank posterior is above
+    the threshold, tested in the log domain in fp32: lp[b, t, blank] (widened
+    to fp32) > fp32(log(threshold)), the log taken in double.  Returns the
+    kept rows of each lane in order (original dtype) and their frame indices.
+    """
+    lthr = np.float32(np.log(np.float64(threshold)))
+    rows, frames = [], []
+    for b in range(len(lens)):
+        n = int(lens[b])
+        lpb = np.asarray(lp[b][:n])
+        keep = ~(lpb[:, blank].astype(np.float32) > lthr)
+        idx = np.nonzero(keep)[0].astype(np.int32)
+        rows.append(lpb[idx])
+        frames.append(idx)
+    return rows, frames
+

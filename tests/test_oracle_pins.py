@@ -387,3 +387,32 @@ def test_work_counters_closed_forms():
                                np.array([-np.inf, -np.inf, -np.inf, 0.0], np.float32))
     st3 = oracle.decode(oracle.Graph(g3), lp, 1, _p(search_beam=1e30))["stats"]
     assert st3["eps_relaxed"] == 4 and st3["sum_m"] == 0 and st3["finals"] == 0
+
+
+def test_blank_skip_rule_by_hand():
+    """Blank-skip pre-slicing (§3: blank-skip stays outside the decoder,
+    WeNet-style, threshold 0.98): a frame is dropped when its blank posterior
+    is above the threshold.  Expected frames written out from the posteriors."""
+    import oracle
+    thr = 0.98
+    lthr = np.float32(np.log(0.98))
+    p_blank = [0.99, 0.97, 0.985, 0.5, 0.999]          # frame 4 lies past lens[0]
+    V = 3
+    lp = np.zeros((2, 6, V), np.float32)
+    for t, pb in enumerate(p_blank):
+        rest = (1.0 - pb) / (V - 1)
+        lp[0, t] = np.log([pb, rest, rest])
+    lp[0, 5] = [lthr, -1.0, -1.0]                      # exactly at log(threshold): kept (strict '>')
+    lens = np.array([4, 0], np.int32)
+    rows, frames = oracle.blank_skip(lp, lens, thr)
+    assert list(frames[0]) == [1, 3]
+    assert np.array_equal(rows[0], lp[0, [1, 3]])
+    assert len(frames[1]) == 0 and rows[1].shape == (0, V)
+    lens = np.array([6, 6], np.int32)
+    lp[1, :, 0] = np.nextafter(lthr, np.float32(0.0))  # just above log(threshold): dropped
+    rows, frames = oracle.blank_skip(lp, lens, thr)
+    assert list(frames[0]) == [1, 3, 5]
+    assert len(frames[1]) == 0
+    # threshold 1: no log-probability lies above log(1) = 0, every frame is kept
+    rows, frames = oracle.blank_skip(lp, lens, 1.0)
+    assert [list(f) for f in frames] == [list(range(6)), list(range(6))]

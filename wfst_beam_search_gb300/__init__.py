@@ -36,7 +36,7 @@ LAT_DTYPE = np.dtype([("t", "<i4"), ("src_state", "<i4"), ("dst_state", "<i4"),
 EXPORTED = ["wfst_graph_upload", "wfst_graph_info", "wfst_graph_free", "wfst_decoder_create",
             "wfst_decoder_free", "wfst_decode", "wfst_lattice_export", "wfst_stream_create",
             "wfst_stream_advance", "wfst_stream_finalize", "wfst_stream_release", "wfst_stats",
-            "wfst_decode_static", "wfst_mem_stats", "wfst_last_error"]
+            "wfst_decode_static", "wfst_mem_stats", "wfst_blank_skip", "wfst_last_error"]
 
 
 class WfstError(RuntimeError):
@@ -105,6 +105,7 @@ def load(build_if_missing: bool = False):
         L.wfst_stream_release.argtypes = [P, i32]
         L.wfst_stats.argtypes = [P, P, i32]
         L.wfst_mem_stats.argtypes = [P, P, i32]
+        L.wfst_blank_skip.argtypes = [P, i32, i64, i64, i32, i32, C.c_float, P, i32, i32, P, P, P, P]
         for name in EXPORTED:
             if name not in ("wfst_last_error", "wfst_graph_free", "wfst_decoder_free"):
                 getattr(L, name).restype = C.c_int
@@ -227,6 +228,32 @@ def wfst_mem_stats(h):
     out = np.zeros(len(MEM_NAMES), np.int64)
     _check(load().wfst_mem_stats(h, _ptr(out), len(MEM_NAMES)))
     return dict(zip(MEM_NAMES, out.tolist()))
+
+
+def wfst_blank_skip(lp_ptr, dtype, stride_b, stride_t, vocab_size, blank_id, threshold, lens_ptr, B, T,
+                    out_ptr, out_lens_ptr, frame_map_ptr, stream):
+    _check(load().wfst_blank_skip(lp_ptr, dtype, stride_b, stride_t, vocab_size, blank_id,
+                                  float(threshold), lens_ptr, B, T, out_ptr, out_lens_ptr,
+                                  frame_map_ptr, stream))
+
+
+def blank_skip(lp, lens, threshold=0.98, blank_id=0, stream=None):
+    """Blank-skip frame pre-slicing of a CUDA [B, T, V] log-prob tensor
+    (a pre-pass outside the decoder).  Returns (out [B, T, V] packed kept
+    rows, out_lens [B] int32, frame_map [B, T] int32), all CUDA tensors; the
+    kernels run on `stream` (torch's current stream if None)."""
+    import torch
+    ptr, dt, sb, st, B, T = _lp_args(lp)
+    V = int(lp.shape[2])
+    dev = lp.device
+    lens_d = torch.as_tensor(np.ascontiguousarray(lens, dtype=np.int32)).to(dev)
+    out = torch.empty((B, T, V), dtype=lp.dtype, device=dev)
+    out_lens = torch.empty(B, dtype=torch.int32, device=dev)
+    fmap = torch.empty((B, T), dtype=torch.int32, device=dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    wfst_blank_skip(ptr, dt, sb, st, V, int(blank_id), threshold, _ptr(lens_d), B, T, _ptr(out),
+                    _ptr(out_lens), _ptr(fmap), _stream(s))
+    return out, out_lens, fmap
 
 
 # ------------------------------------------------------------ convenience wrappers
