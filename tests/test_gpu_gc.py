@@ -170,3 +170,26 @@ def test_gc_rejects_lattice_and_negative_interval(W):
         W.Decoder(G, W.make_params(lattice=True, gc_interval=8), 1, 16)
     with pytest.raises(W.WfstError, match="INVALID_ARG"):
         W.Decoder(G, W.make_params(gc_interval=-1), 1, 16)
+
+
+def test_gc_channel_reuse_and_ragged_channels(W):
+    """Two channels of one GC decoder with different lengths, released and
+    opened again for a second pair of streams: each stream starts from an
+    empty finalized list and a fresh root, and every partial and final result
+    equals the oracle's."""
+    wl = synth.workload(0)
+    g = synth.make_graph(0)
+    p = wl_params(wl, lattice=False)
+    G = W.Graph(g, device=0)
+    D = W.Decoder(G, _params(W, p, True, 16), 2, 16, W.Capacity(0, 1 << 16, 0, 4096, 0))
+    OG = oracle.Graph(g)
+    for rnd, T in enumerate((3000, 1000)):
+        lp = np.stack([synth.make_lane_log_probs(0, 10 + 2 * rnd + i, T=T) for i in range(2)])
+        lens = np.array([T, T // 2 + 3], np.int32)
+        chans = [D.stream_create(), D.stream_create()]
+        partials, final = _stream(W, D, lp, lens, 16, chans)
+        for i in range(2):
+            parts, r, _ = _oracle_stream(OG, p, lp[i], int(lens[i]), 16, T)
+            _check_stream(partials, final, i, parts, r, f"round {rnd} channel {i}", every=7)
+        for c in chans:
+            D.stream_release(c)
