@@ -14,15 +14,17 @@
 //   §5.3 pass 1 (max): exact per-lane maximum of end = (score + w) + lp over
 //        every slot, skipping tokens whose upper bound (score + max weight) +
 //        max log-prob cannot beat an end already posted; pass 2 (expand):
-//        admit end > max - beam and recombine by destination with one 64-bit
-//        atomicMax on (ordered score, lowest arc id) — a direct-indexed
-//        per-lane table replaces the page's hash;
-//   §5.4 commit: each frontier token gets a winners-log entry {prev, arc};
+//        admit end > max - beam and recombine by destination with a 128-bit
+//        CAS on {(ordered score, lowest arc id), source token} — a
+//        direct-indexed per-lane table replaces the page's hash;
+//   §5.4 commit: each frontier token gets a winners-log entry {delta, arc}
+//        (its predecessor is the entry delta places back);
 //   §5.5 epsilon closure by worklist passes to a fixpoint; lattice records;
 //   §7  backtrack from the final token; lattice backward output_beam prune.
-// Work distribution: the arc slots of a frame form tiles of kTile slots; each
-// warp walks its own tiles with no block-level synchronisation, staging the
-// tiles' tokens in its own shared-memory area, and every lane issues the
+// Work distribution: the arc slots of a frame form tiles of kTile slots; a
+// CTA owns every (G*W)-th group of W adjacent tiles (W warps per CTA) and
+// hands them, in order, to whichever of its warps is free; a warp stages its
+// tile's tokens in its own shared-memory area, and every lane issues the
 // loads of its kSPT slots together (one chain of dependent accesses per tile).
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -128,9 +130,6 @@ __device__ __forceinline__ unsigned lanemask_lt() {
   unsigned m;
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
   return m;
-}
-__device__ __forceinline__ void prefetch_l1(const void* p) {
-  asm volatile("prefetch.global.L1 [%0];" : : "l"(p));
 }
 __device__ __forceinline__ TokRec ld_tok(const TokRec* p) {
   const int4 v = __ldcg(reinterpret_cast<const int4*>(p));
@@ -319,11 +318,6 @@ __device__ __forceinline__ ulonglong2* ent_at(const DevWork& w, int l, int32_t d
   return w.ent + ((((size_t)l * (size_t)w.N + (size_t)d) << 1) | (size_t)par);
 }
 
-__device__ __forceinline__ unsigned long long ld_relaxed_u64(const void* p) {
-  unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
 
 __device__ __forceinline__ ulonglong2 cas128(ulonglong2* p, ulonglong2 cmp, ulonglong2 val) {
   ulonglong2 old;
@@ -576,7 +570,7 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
             if (!a.lattice && p < own_hi && (p > p_lo || k == 0))
               *ent_at(w, l, tr.state, par) = make_ulonglong2(0ull, 0ull);
             if (s.need_commit && p < own_hi) {
-              // commit (§5.4): the winners-log entry {prev, arc} of the token
+              // commit (§5.4): the winners-log entry {delta, arc} of the token
               const int32_t arc = key_id(e.x);
               const uint32_t src = ent_src(e);
               const int64_t base_new = s.cursor, base_old = s.base_cur;
@@ -1403,7 +1397,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
       }
     }
     {  // commit (§5.4) of final / partial lanes and of frames without
-       // emitting arcs: winners-log entry {prev, arc} per token; final-step
+       // emitting arcs: winners-log entry {delta, arc} per token; final-step
        // keys and the best token
       const int total = S.pre_b[L];
       const int wlane = tid & 31;
