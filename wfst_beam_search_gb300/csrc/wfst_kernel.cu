@@ -481,22 +481,29 @@ __device__ __forceinline__ void warp_claim(const RunArgs& a, const bool (&want)[
   }
 }
 
-// Warp-cooperative lattice record append.
-__device__ __forceinline__ void warp_lat_append(const RunArgs& a, bool want, int l, const LatRec& r) {
-  const DevWork& w = a.w;
+// Warp-cooperative lattice record append: one 64-bit atomic reserves the
+// records of all K slots of every thread (ballot m[k] per slot); the record
+// of slot k of this thread goes to base + sum_{k' < k} popc(m[k']) +
+// popc(m[k] & lanemask_lt) (lat_put).  The backward prune treats the records
+// of a frame's group in any order.
+template <int K>
+__device__ __forceinline__ unsigned long long warp_lat_reserve(const RunArgs& a, const bool (&want)[K], int l,
+                                                               unsigned (&m)[K]) {
   const unsigned full = 0xffffffffu;
-  const unsigned m = __ballot_sync(full, want);
-  if (!m) return;
-  const int lane = threadIdx.x & 31;
-  const int ld = __ffs(m) - 1;
-  unsigned long long b = 0;
-  if (lane == ld) b = atomicAdd(&w.lat_cnt[l], (unsigned long long)__popc(m));
-  b = __shfl_sync(full, b, ld);
-  if (want) {
-    const unsigned long long p = b + __popc(m & lanemask_lt());
-    if (p < (unsigned long long)w.lat_cap) w.lat[(size_t)l * w.lat_cap + p] = r;
-    else lane_ovf(a, l, kOvfArena);
+  uint32_t tot = 0;
+#pragma unroll
+  for (int k = 0; k < K; k++) {
+    m[k] = __ballot_sync(full, want[k]);
+    tot += __popc(m[k]);
   }
+  unsigned long long b = 0;
+  if (tot && (threadIdx.x & 31) == 0) b = atomicAdd(&a.w.lat_cnt[l], (unsigned long long)tot);
+  return __shfl_sync(full, b, 0);
+}
+__device__ __forceinline__ void lat_put(const RunArgs& a, int l, unsigned long long p, const LatRec& r) {
+  const DevWork& w = a.w;
+  if (p < (unsigned long long)w.lat_cap) w.lat[(size_t)l * w.lat_cap + p] = r;
+  else lane_ovf(a, l, kOvfArena);
 }
 
 // ------------------------------------------------------------------ emitting tiles
@@ -673,18 +680,24 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
           }
         }
         if (a.lattice) {
+          unsigned lm[kSPT];
+          unsigned long long lb = warp_lat_reserve<kSPT>(a, adm, l, lm);
+          const unsigned lt = lanemask_lt();
 #pragma unroll
           for (int j = 0; j < kSPT; j++) {
-            LatRec r;
-            r.frame_flags = f << 4;
-            r.src_tok = (int32_t)(s.base_cur + (c + ti[j]));
-            r.dst_tok = -1;
-            r.src_state = ws.state[ti[j]];
-            r.dst_state = d[j];
-            r.arc = id[j];
-            r.end = end[j];
-            r.arcscore = wt[j];
-            warp_lat_append(a, adm[j], l, r);
+            if (adm[j]) {
+              LatRec r;
+              r.frame_flags = f << 4;
+              r.src_tok = (int32_t)(s.base_cur + (c + ti[j]));
+              r.dst_tok = -1;
+              r.src_state = ws.state[ti[j]];
+              r.dst_state = d[j];
+              r.arc = id[j];
+              r.end = end[j];
+              r.arcscore = wt[j];
+              lat_put(a, l, lb + __popc(lm[j] & lt), r);
+            }
+            lb += __popc(lm[j]);
           }
         }
 #pragma unroll
@@ -780,18 +793,24 @@ __device__ void eps_tiles(const RunArgs& a, Smem& S, int buf, int next_slot) {
         if (!adm[j]) d[j] = id[j] = 0;
       }
       if (a.lattice) {
+        unsigned lm[kSPT];
+        unsigned long long lb = warp_lat_reserve<kSPT>(a, adm, l, lm);
+        const unsigned lt = lanemask_lt();
 #pragma unroll
         for (int j = 0; j < kSPT; j++) {
-          LatRec r;
-          r.frame_flags = (fr << 4) | kRecEps;
-          r.src_tok = __float_as_int(ws.score[ti[j]]);  // score used; checked at resolution
-          r.dst_tok = -1;
-          r.src_state = ws.state[ti[j]];
-          r.dst_state = d[j];
-          r.arc = id[j];
-          r.end = e[j];
-          r.arcscore = wt[j];
-          warp_lat_append(a, adm[j], l, r);
+          if (adm[j]) {
+            LatRec r;
+            r.frame_flags = (fr << 4) | kRecEps;
+            r.src_tok = __float_as_int(ws.score[ti[j]]);  // score used; checked at resolution
+            r.dst_tok = -1;
+            r.src_state = ws.state[ti[j]];
+            r.dst_state = d[j];
+            r.arc = id[j];
+            r.end = e[j];
+            r.arcscore = wt[j];
+            lat_put(a, l, lb + __popc(lm[j] & lt), r);
+          }
+          lb += __popc(lm[j]);
         }
       }
       bool claim[kSPT], better[kSPT];
