@@ -1332,7 +1332,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
       S.pre_a[l] = S.pre_b[l] = S.pre_c[l] = S.pre_d[l] = 0;
       s.res_lo = s.res_hi = 0;
       if (s.row < 0 || s.status != kLaneRunning) continue;
-      if (s.was_emit) s.sum_m += __ldcg(&fc_of(w, s.t, l)->cnt) >> 32;
+      // the step's global reads, issued together
+      const unsigned long long cnt = __ldcg(&fc_of(w, s.t, l)->cnt);
+      const unsigned long long cp = s.t >= 1 ? __ldcg(&fc_of(w, s.t - 1, l)->cnt) : 0ull;
+      const float mlp = s.t < s.t_end ? __ldcg(w.maxlp + (size_t)l * w.max_frames + (s.t - s.t0)) : 0.f;
+      if (s.was_emit) s.sum_m += cnt >> 32;
       s.was_emit = 0;
       if (s.gc_due) {  // a GC round of the last step moved the root and finalized words
         s.floor = __ldcg(&w.lanes[l].floor);
@@ -1343,7 +1347,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
       else if ((s.flags & kCallFinal) && !s.done_final) s.phase = kFin;
       else if ((s.flags & kCallPartial) && !(s.flags & kCallFinal) && !s.done_partial) s.phase = kPart;
       if (s.phase == kNone) continue;
-      const unsigned long long cnt = __ldcg(&fc_of(w, s.t, l)->cnt);
       const unsigned long long n_raw = cnt >> 32;
       s.n_cur = (int32_t)min(n_raw, (unsigned long long)w.qcap);
       s.d_cur = (uint32_t)cnt;
@@ -1354,10 +1357,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         s.d_cur = r.off + (uint32_t)(m.y - m.x);
       }
       s.n_prev = 0;
-      if (s.t >= 1 && s.phase != kPart) {
-        const unsigned long long cp = __ldcg(&fc_of(w, s.t - 1, l)->cnt);
-        s.n_prev = (int32_t)min(cp >> 32, (unsigned long long)w.qcap);
-      }
+      if (s.t >= 1 && s.phase != kPart) s.n_prev = (int32_t)min(cp >> 32, (unsigned long long)w.qcap);
       s.need_commit = (s.committed < s.t) ? 1 : 0;
       if (s.phase == kEmit) {
         // dynamic beam (§3 "Dynamic beam")
@@ -1377,7 +1377,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         s.frames += 1;
         s.sum_n += n_raw;
         s.sum_d += s.d_cur;
-        s.maxlp = __ldcg(w.maxlp + (size_t)l * w.max_frames + (s.t - s.t0));
+        s.maxlp = mlp;
       }
       // the commit loop: final / partial lanes, and frames without emitting
       // arcs (no tiles); the max pass commits every other frame
