@@ -168,8 +168,11 @@ void wfst_decoder_free(wfst_decoder* d);
  * `dtype`, element (b, t, v) at log_probs[b*stride_b + t*stride_t + v]
  * (unit stride over v, stride_t >= V).  It may be a device pointer (read in
  * place) or a host pointer (copied to device inside the call).  lens: host
- * [B], 0 <= lens[b] <= T.  Requires B <= max_lanes, T <= max_frames and a
- * decoder created with streaming = 0.
+ * [B], 0 <= lens[b] <= T.  Requires B <= max_lanes and a decoder created with
+ * streaming = 0.  T above max_frames first grows the decoder's per-frame
+ * tables to max(T, 2 * max_frames) (§6 frame-capacity doubling; the
+ * best-path buffer grows with them while it has its default size), unless
+ * the decoder was created with WFST_OPT_NO_GROW (then INVALID_ARG).
  * Outputs (host, caller-allocated): words [B*words_cap] (lane b's words at
  * b*words_cap, forward order), word_lens [B] (TRUE length, may exceed
  * words_cap: re-issue with a larger buffer), scores [B] (fp32 path score
@@ -260,7 +263,8 @@ int wfst_stats(wfst_decoder* d, int64_t* out, int32_t n);
  * Workspace of a decoder (host int64, n entries written, at most
  * WFST_MEM_COUNT): device bytes held, then the current per-lane capacities
  * (frontier tokens, winners-log entries, lattice records, best-path arcs) and
- * the number of capacity doublings so far.  §6.2 of the page reports the
+ * the number of capacity doublings so far, then max_frames (which offline
+ * decodes of longer utterances raise).  §6.2 of the page reports the
  * decoder's memory the same way; here capacities only grow on demand.
  */
 #define WFST_MEM_BYTES 0
@@ -269,7 +273,8 @@ int wfst_stats(wfst_decoder* d, int64_t* out, int32_t n);
 #define WFST_MEM_LATTICE_CAP 3
 #define WFST_MEM_PATH_CAP 4
 #define WFST_MEM_GROWS 5
-#define WFST_MEM_COUNT 6
+#define WFST_MEM_MAX_FRAMES 6    /* frames per call the per-frame tables hold now */
+#define WFST_MEM_COUNT 7
 int wfst_mem_stats(wfst_decoder* d, int64_t* out, int32_t n);
 
 /*

@@ -310,6 +310,37 @@ def test_capacities_grow_until_results_are_exact(W, graphs):
         G.close()
 
 
+def test_frame_capacity_grows_for_longer_utterances(W, graphs):
+    """Utterances longer than the decoder's max_frames grow its per-frame
+    tables (the page's frame-capacity doubling): workload 1 decoded at T=200
+    on a decoder made for 24 frames, and workload 0 with its lattice at T=50
+    on one made for 8 frames, equal the oracle; with growth turned off the
+    call is refused."""
+    for wi, T, mf in ((1, 200, 24), (0, 50, 8)):
+        wl = synth.workload(wi)
+        g = graphs(wi)
+        lanes = list(range(3))
+        lp = synth.make_log_probs(wi, lanes=lanes, T=T)
+        lens = np.array([T, T // 2, 1], np.int32)
+        p = wl_params(wl, lattice=(wi == 0))
+        G, D = gpu_decoder(W, g, p, len(lanes), mf)
+        assert D.mem_stats()["max_frames"] == mf
+        out = D.decode(_cuda(lp), lens)
+        assert D.mem_stats()["max_frames"] >= T
+        OG = oracle.Graph(g)
+        for b in range(len(lanes)):
+            ref = oracle_lane(OG, lp[b], lens[b], p)
+            assert_lane_equal(out[b], ref, f"workload {wi} lane {b}")
+            if p["lattice"] and ref["ok"]:
+                assert_lattice_equal(D.lattice(b), ref["lattice"], f"workload {wi} lane {b}")
+        D.close()
+        _, D0 = gpu_decoder(W, g, p, len(lanes), mf, graph=G, options=W.OPT_NO_GROW)
+        with pytest.raises(W.WfstError, match="INVALID_ARG"):
+            D0.decode(_cuda(lp), lens)
+        D0.close()
+        G.close()
+
+
 # ------------------------------------------------------------ maximum sizes, degenerate graphs
 
 def test_max_lanes_256(W):

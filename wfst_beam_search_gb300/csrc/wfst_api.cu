@@ -259,6 +259,7 @@ struct wfst_decoder {
   std::vector<size_t> alloc_bytes;
   int64_t bytes = 0;
   int64_t grows = 0;              // capacity doublings so far
+  bool path_default = true;       // the best-path buffer has its default size (follows max_frames)
   // pinned host mirrors
   LaneCall* h_calls = nullptr;
   Result* h_res = nullptr;
@@ -382,6 +383,7 @@ extern "C" int wfst_decoder_create(wfst_graph* g, const wfst_params* params, int
   d->p = *params;
   d->L = max_lanes;
   d->max_frames = max_frames;
+  d->path_default = !(caps && caps->path_cap > 0);
   DeviceGuard dgd(g->device);
   DevWork& w = d->w;
   w.L = max_lanes;
@@ -707,6 +709,44 @@ static int grow_capacities(wfst_decoder* d, bool g_log, bool g_lat, bool g_q, bo
   return WFST_OK;
 }
 
+// Offline frame-capacity growth (the page's §6 "frame-capacity doubling"):
+// an utterance longer than max_frames grows the per-frame tables (row
+// maxima, lattice group bounds, per-frame path marks) to max(T, 2 *
+// max_frames), and the best-path buffer with them while it has its default
+// size.  Every new array is allocated before an old one is released.
+static int grow_frames(wfst_decoder* d, int32_t T) {
+  DevWork& w = d->w;
+  const size_t L = (size_t)d->L;
+  const DevGraph& G = d->g->dg;
+  const int64_t nf64 = std::max<int64_t>(T, std::min<int64_t>(2 * (int64_t)d->max_frames, (int64_t)INT32_MAX / 8));
+  if (nf64 > (int64_t)INT32_MAX / 8) return fail(WFST_ERR_CAPACITY, "decode: T is too large for the frame tables");
+  const int32_t nf = (int32_t)nf64;
+  const size_t mf = (size_t)nf + 2;
+  int64_t path_cap = w.path_cap;
+  if (d->path_default) path_cap = std::max<int64_t>(path_cap, 4 * (int64_t)mf * (1 + (int64_t)G.eps_depth));
+  struct Plan { void** slot; size_t bytes; void* fresh; bool zero; };
+  Plan plan[4];
+  int np = 0;
+  plan[np++] = {(void**)&w.maxlp, sizeof(float) * L * (size_t)std::max(nf, 1), nullptr, false};
+  plan[np++] = {(void**)&w.pframe, sizeof(int2) * L * mf, nullptr, false};
+  if (w.lattice) plan[np++] = {(void**)&w.lat_groups, sizeof(int64_t) * L * mf, nullptr, true};
+  if (path_cap != w.path_cap) plan[np++] = {(void**)&w.path, sizeof(int32_t) * L * (size_t)path_cap, nullptr, false};
+  for (int i = 0; i < np; i++) {
+    if (cudaMalloc(&plan[i].fresh, plan[i].bytes) != cudaSuccess ||
+        (plan[i].zero && cudaMemset(plan[i].fresh, 0, plan[i].bytes) != cudaSuccess)) {
+      cudaGetLastError();
+      if (plan[i].fresh) cudaFree(plan[i].fresh);
+      for (int k = 0; k < i; k++) cudaFree(plan[k].fresh);
+      return fail(WFST_ERR_OOM, "decode: no device memory to grow the frame tables");
+    }
+  }
+  for (int i = 0; i < np; i++) dswap(d, plan[i].slot, plan[i].fresh, plan[i].bytes);
+  d->max_frames = nf;
+  w.max_frames = nf;
+  w.path_cap = path_cap;
+  return WFST_OK;
+}
+
 static void stats_add(int64_t* acc, const int64_t* s) {
   for (int i = 0; i < WFST_STAT_COUNT; i++)
     acc[i] = (i == WFST_STAT_STEPS) ? std::max(acc[i], s[i]) : acc[i] + s[i];
@@ -720,7 +760,9 @@ extern "C" int wfst_decode(wfst_decoder* d, const void* log_probs, int32_t dtype
   std::lock_guard<std::mutex> lock(d->mu);
   if (d->p.streaming) return fail(WFST_ERR_STATE, "decode: the decoder was created for streaming");
   if (B < 0 || B > d->L) return fail(WFST_ERR_INVALID_ARG, "decode: B must lie in [0, max_lanes]");
-  if (T < 0 || T > d->max_frames) return fail(WFST_ERR_INVALID_ARG, "decode: T must lie in [0, max_frames]");
+  if (T < 0) return fail(WFST_ERR_INVALID_ARG, "decode: T must be >= 0");
+  if (T > d->max_frames && (d->p.options & WFST_OPT_NO_GROW))
+    return fail(WFST_ERR_INVALID_ARG, "decode: T exceeds max_frames (the decoder was created with WFST_OPT_NO_GROW)");
   if (dtype != WFST_F32 && dtype != WFST_F16) return fail(WFST_ERR_INVALID_ARG, "decode: dtype must be F32 or F16");
   if (words_cap < 0 || (words_cap > 0 && !words)) return fail(WFST_ERR_INVALID_ARG, "decode: bad words buffer");
   if (B == 0) return WFST_OK;
@@ -736,6 +778,11 @@ extern "C" int wfst_decode(wfst_decoder* d, const void* log_probs, int32_t dtype
       return fail(WFST_ERR_INVALID_ARG, "decode: stride_t must be >= vocab_size and stride_b >= 0");
   }
   DeviceGuard dgd(d->g->device);
+  if (T > d->max_frames) {
+    CU(cudaStreamSynchronize((cudaStream_t)stream), "decode: wait before growing the frame tables");
+    const int rg = grow_frames(d, T);
+    if (rg != WFST_OK) return rg;
+  }
   cudaStream_t st = (cudaStream_t)stream;
   const void* lp = log_probs;
   int rc = stage_input(d, log_probs, dtype, stride_b, stride_t, B, T, st, &lp);
@@ -1002,7 +1049,8 @@ extern "C" int wfst_stream_release(wfst_decoder* d, int32_t channel) {
 extern "C" int wfst_mem_stats(wfst_decoder* d, int64_t* out, int32_t n) {
   if (!d || !out || n < 0) return fail(WFST_ERR_INVALID_ARG, "mem_stats: bad argument");
   std::lock_guard<std::mutex> lock(d->mu);
-  const int64_t v[WFST_MEM_COUNT] = {d->bytes, d->w.qcap, d->w.log_cap, d->w.lat_cap, d->w.path_cap, d->grows};
+  const int64_t v[WFST_MEM_COUNT] = {d->bytes, d->w.qcap, d->w.log_cap, d->w.lat_cap, d->w.path_cap, d->grows,
+                                     d->max_frames};
   for (int32_t i = 0; i < n && i < WFST_MEM_COUNT; i++) out[i] = v[i];
   return WFST_OK;
 }
