@@ -141,6 +141,16 @@ __device__ __forceinline__ TokRec ld_tok(const TokRec* p) {
   return r;
 }
 
+// An arc record read by the expand pass or an epsilon pass: read-only, and
+// read once in the pass, so it is kept out of L1 (which then holds the
+// log-prob rows and token rows the same tiles reuse).
+__device__ __forceinline__ int4 ld_arc(const int4* p) {
+  int4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.s32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
 template <typename T>
 __device__ __forceinline__ float lp_at(const T* row, int v);
 template <>
@@ -629,7 +639,7 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
           wt[j] = __int_as_float(r.y);
           d[j] = id[j] = 0;
         } else {
-          const int4 r = act[j] ? __ldg(g.arcs + ai[j]) : make_int4(0, 0, 0, 0);
+          const int4 r = act[j] ? ld_arc(g.arcs + ai[j]) : make_int4(0, 0, 0, 0);
           d[j] = r.x;
           wt[j] = __int_as_float(r.y);
           il[j] = r.z;
@@ -781,7 +791,7 @@ __device__ void eps_tiles(const RunArgs& a, Smem& S, int buf, int next_slot) {
       int32_t d[kSPT], id[kSPT];
 #pragma unroll
       for (int j = 0; j < kSPT; j++) {
-        const int4 r = act[j] ? __ldg(g.arcs + ai[j]) : make_int4(0, 0, 0, 0);
+        const int4 r = act[j] ? ld_arc(g.arcs + ai[j]) : make_int4(0, 0, 0, 0);
         d[j] = r.x;
         wt[j] = __int_as_float(r.y);
         id[j] = r.w;
