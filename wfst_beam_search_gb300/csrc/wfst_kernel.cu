@@ -151,6 +151,17 @@ __device__ __forceinline__ int4 ld_arc(const int4* p) {
   return v;
 }
 
+// The max pass's read of a token's recombination entry, with an L2
+// evict-last policy: a state that stays in the beam (a blank self-loop) has
+// its entry's line taken by the next expand pass's CAS.
+__device__ __forceinline__ ulonglong2 ld_ent_keep(const ulonglong2* p) {
+  unsigned long long pol;
+  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  ulonglong2 v;
+  asm volatile("ld.global.cg.L2::cache_hint.v2.u64 {%0, %1}, [%2], %3;" : "=l"(v.x), "=l"(v.y) : "l"(p), "l"(pol));
+  return v;
+}
+
 template <typename T>
 __device__ __forceinline__ float lp_at(const T* row, int v);
 template <>
@@ -389,7 +400,8 @@ __device__ __forceinline__ void wlog_commit(const RunArgs& a, int l, int64_t idx
   const DevWork& w = a.w;
   const int64_t d = arc < 0 ? 0 : idx - prev;
   const int32_t x = a.gc_interval > 0 ? (int32_t)((uint32_t)d & kDeltaMask) : (int32_t)d;
-  if (idx - floor < w.log_cap) *wlog_at(w, l, idx) = make_int2(x, arc);
+  // a streaming store: the entry is read again only by a backtrack or a GC
+  if (idx - floor < w.log_cap) __stcs(wlog_at(w, l, idx), make_int2(x, arc));
   else lane_ovf(a, l, kOvfArena);
 }
 // Token positions per state are kept only where something looks a state's
@@ -577,7 +589,7 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
           const TokRec tr = ld_tok(w.front + q + c + i);
           float sc;
           if (MODE == 0) {
-            const ulonglong2 e = __ldcg(ent_at(w, l, tr.state, par));
+            const ulonglong2 e = ld_ent_keep(ent_at(w, l, tr.state, par));
             sc = key_score(e.x);
             w.score[q + c + i] = sc;
             const int32_t p = c + i;
