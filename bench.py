@@ -23,6 +23,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -32,8 +33,11 @@ sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
 
-# SURVEY-defined algorithmic bytes per lane-step (n: frontier, D: emitting
-# arcs, a: admitted candidates, m: next frontier), plus one log-prob row.
+# Algorithmic bytes per lane-step (n: frontier tokens, D: their emitting
+# arcs, a: admitted candidates, m: next-frontier tokens), plus one log-prob
+# row: a token's state, score and row bounds (20 B), an arc's label and
+# weight (6 B), an admitted candidate's destination and recombination entry
+# (16 B), a new token's record, winners-log entry and cleared entry (32 B).
 BYTES_N, BYTES_D, BYTES_A, BYTES_M = 20, 6, 16, 32
 
 
@@ -83,7 +87,7 @@ class Clocks:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"wfst_bench_clocks_{os.getpid()}.csv")
 
     def start(self):
         try:
