@@ -151,6 +151,9 @@ __device__ __forceinline__ int4 ld_arc(const int4* p) {
   return v;
 }
 
+__device__ __forceinline__ void prefetch_l2_keep(const void* p) {
+  asm volatile("prefetch.global.L2::evict_last [%0];" : : "l"(p));
+}
 // The max pass's read of a token's recombination entry, with an L2
 // evict-last policy: a state that stays in the beam (a blank self-loop) has
 // its entry's line taken by the next expand pass's CAS.
@@ -722,6 +725,12 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
             lb += __popc(lm[j]);
           }
         }
+        // the admitted candidates' entry lines, marked evict-last in L2: the
+        // next max pass reads them again (and the next expand pass's CAS, for
+        // a state that stays in the beam)
+#pragma unroll
+        for (int j = 0; j < kSPT; j++)
+          if (adm[j]) prefetch_l2_keep(ent_at(w, l, d[j], par ^ 1));
 #pragma unroll
         for (int j = 0; j < kSPT; j++) {
           claim[j] = adm[j] && relax_ent(a, ent_at(w, l, d[j], par ^ 1), mk_key(end[j], id[j]),
@@ -836,6 +845,9 @@ __device__ void eps_tiles(const RunArgs& a, Smem& S, int buf, int next_slot) {
         }
       }
       bool claim[kSPT], better[kSPT];
+#pragma unroll
+      for (int j = 0; j < kSPT; j++)
+        if (adm[j]) prefetch_l2_keep(ent_at(w, l, d[j], par));
 #pragma unroll
       for (int j = 0; j < kSPT; j++) {
         const int r = adm[j] ? relax_ent(a, ent_at(w, l, d[j], par), mk_key(e[j], id[j]),
