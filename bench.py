@@ -343,7 +343,7 @@ def run_gpu(args):
                    "global_batch": B * ws, "frames_per_utt": T, "vocab": wl.V, "log_probs": wl.dtype,
                    "search_beam": wl.search_beam, "max_active": wl.max_active,
                    "min_active": wl.min_active, "parallelism": f"replicas x{ws} (lanes sharded)",
-                   "l2": "inputs larger than L2 (320 MB log-probs, 218 MB graph); no flush",
+                   "l2": "inputs larger than L2 (320 MB log-probs, 320 MB graph, ~15 GB workspace); no flush",
                    "mode": (f"streaming: {wl.chunk}-frame chunks, partial per chunk, finalize with lattice"
                             if wl.streaming else "offline"),
                    "gc_interval": args.gc_interval},
