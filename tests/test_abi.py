@@ -101,3 +101,32 @@ def test_binding_structs_match_the_header(tmp_path):
         assert got[(cname, "size")] == C.sizeof(py), cname
         for f, _ in py._fields_:
             assert got[(cname, f)] == getattr(py, f).offset, (cname, f)
+
+
+def test_blank_skip_argument_checks_without_gpu(lib):
+    """wfst_blank_skip validates its arguments on the host before any launch:
+    NULL arrays, a blank id outside [0, V), a non-positive threshold, short
+    strides and host (not device) arrays are refused with INVALID_ARG."""
+    import ctypes as C
+    import numpy as np
+    lp = np.zeros((2, 3, 4), np.float32)
+    lens = np.array([3, 3], np.int32)
+    out = np.zeros_like(lp)
+    out_lens = np.zeros(2, np.int32)
+    fmap = np.zeros((2, 3), np.int32)
+    P = lambda a: a.ctypes.data_as(C.c_void_p)  # noqa: E731
+    f = lib.wfst_blank_skip
+    base = dict(lp=P(lp), dt=0, sb=12, st=4, V=4, blank=0, thr=C.c_float(0.98), lens=P(lens), B=2, T=3,
+                out=P(out), ol=P(out_lens), fm=P(fmap))
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return f(a["lp"], a["dt"], a["sb"], a["st"], a["V"], a["blank"], a["thr"], a["lens"], a["B"], a["T"],
+                 a["out"], a["ol"], a["fm"], None)
+    assert call(B=0) == 0                      # nothing to do
+    assert call(lp=None) == -1 and b"NULL" in lib.wfst_last_error()
+    assert call(blank=4) == -1 and b"blank_id" in lib.wfst_last_error()
+    assert call(thr=C.c_float(0.0)) == -1 and b"threshold" in lib.wfst_last_error()
+    assert call(st=3) == -1 and b"stride" in lib.wfst_last_error()
+    assert call(dt=7) == -1 and b"dtype" in lib.wfst_last_error()
+    assert call() == -1 and b"device memory" in lib.wfst_last_error()   # host arrays
