@@ -52,7 +52,8 @@ extern "C" {
 /* ---- per-lane overflow bits (meta[3*b + 2]; §7 "Overflow bits") ------- */
 #define WFST_OVF_ARENA 4     /* winners log or lattice arena full            */
 #define WFST_OVF_KEPT 16     /* surviving frontier larger than frontier_cap  */
-#define WFST_OVF_PATH 32     /* best path longer than path_cap (oldest arcs lost) */
+#define WFST_OVF_PATH 32     /* best path longer than path_cap (oldest arcs lost),
+                                or, with the winners-log GC, fin_cap words finalized */
 
 /* ---- lattice record flags -------------------------------------------- */
 #define WFST_REC_EPS 1
