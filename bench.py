@@ -20,6 +20,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -45,15 +46,23 @@ BYTES_N, BYTES_D, BYTES_A, BYTES_M = 20, 6, 16, 32
 # command, from a one-pass ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum; the command is in profiles/).  It describes only the
 # kernel source it was taken on: any change to that source makes it null.
-MEASURED_TRAFFIC = {"kernel_sha256": "e99435c8483dc08ddfd2dfe5071d171ea53dd8fef3ce76a89d77403a463f2bc2",
+MEASURED_TRAFFIC = {"kernel_sha256": "dfb05e9f2cf19657d70e6e65719fc48f08620df41893aa73eca70f5482600b6d",
                     "workload": "hlg-B64xT500xV5000-f16", "lanes": 64, "bytes": 179_810_351_616}
+
+
+def _code_only(text: str) -> str:
+    """The source without comments and blank space, so that a comment edit
+    does not void a measurement of the same code."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(" ".join(line.split()) for line in text.splitlines() if line.strip())
 
 
 def kernel_sha256():
     h = hashlib.sha256()
     for f in ("wfst_kernel.cu", "wfst_internal.h"):
-        with open(os.path.join(ROOT, "wfst_beam_search_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "wfst_beam_search_gb300", "csrc", f)) as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()
 
 

@@ -151,6 +151,8 @@ __device__ __forceinline__ int4 ld_arc(const int4* p) {
   return v;
 }
 
+// Bring a line into L2 with evict-last priority (used for each admitted
+// candidate's entry just before its CAS: the next max pass reads it again).
 __device__ __forceinline__ void prefetch_l2_keep(const void* p) {
   asm volatile("prefetch.global.L2::evict_last [%0];" : : "l"(p));
 }
