@@ -120,3 +120,31 @@ def test_workload4_full_128_channels_sampled(W):
         assert_lattice_equal(D.lattice(channels[i]), lat, f"channel {i} lattice")
     for c in channels:
         D.stream_release(c)
+
+
+def test_streaming_search_matches_oracle_and_restarts_on_overflow(W):
+    """StreamingSearch on real channels: without overflow its per-chunk words
+    and final result are the oracle's streaming results; on a decoder whose
+    frontier capacity is far too small, flagged chunks restart the channel
+    and the stream still ends with a result."""
+    wl = synth.workload(0)
+    g = synth.make_graph(0)
+    T, chunk = 300, 16
+    lp = synth.make_lane_log_probs(0, 3, T=T)
+    p = wl_params(wl, lattice=False)
+    G, D = gpu_decoder(W, g, p, 2, chunk, caps=W.Capacity(0, 0, 0, 4096), streaming=True)
+    s = W.StreamingSearch(D)
+    outs = [s.feed(torch.from_numpy(np.ascontiguousarray(lp[t:t + chunk])).to("cuda:0"))
+            for t in range(0, T, chunk)]
+    f = s.finish()
+    parts, r, _ = _oracle_stream(oracle.Graph(g), p, lp, T, chunk, T)
+    assert f["restarts"] == 0
+    for k, (o, op) in enumerate(zip(outs, parts)):
+        assert o["words"] == list(op["words"]), f"chunk {k}"
+    assert f["words"] == list(r["words"]) and abs(f["score"] - r["score"]) <= SCORE_TOL
+    _, D2 = gpu_decoder(W, g, p, 2, chunk, caps=W.Capacity(4, 0, 0, 4096), graph=G, streaming=True)
+    s2 = W.StreamingSearch(D2)
+    for t in range(0, T, chunk):
+        s2.feed(torch.from_numpy(np.ascontiguousarray(lp[t:t + chunk])).to("cuda:0"))
+    f2 = s2.finish()
+    assert s2.restarts > 0 and isinstance(f2["words"], list)

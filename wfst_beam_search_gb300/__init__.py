@@ -421,3 +421,62 @@ def _stream(s):
     if isinstance(s, int):
         return C.c_void_p(s)
     return C.c_void_p(int(s.cuda_stream))   # torch.cuda.Stream
+
+
+class StreamingSearch:
+    """One stream decoded through a channel of a streaming ``Decoder``, with
+    the caller-side overflow policy of the page "GPU WFST Beam-Search
+    Decoder" (§7 overflow handling, §8.1): a channel whose chunk comes back
+    with a capacity overflow bit set (winners log or frontier: the channel's
+    search state is incomplete) cannot be trusted from then on, so it is
+    abandoned, the hypothesis it gave before that chunk is kept as a finished
+    prefix, and the chunk is decoded again on a fresh channel.  The search
+    context across the burst is lost; the audio after it is not.
+
+    ``feed`` returns the words so far (prefix + the channel's partial
+    hypothesis); ``finish`` runs the final step and releases the channel.
+    Scores are the current channel's (they do not include the prefix)."""
+
+    def __init__(self, decoder, words_cap=4096):
+        self.d = decoder
+        self.words_cap = words_cap
+        self.prefix = []
+        self.last_words = []
+        self.restarts = 0
+        self.ch = self._open()
+
+    def _open(self):
+        ch = self.d.stream_create()
+        if ch < 0:
+            raise RuntimeError("StreamingSearch: every channel of the decoder is busy")
+        return ch
+
+    def _advance(self, lp_chunk, length):
+        return self.d.stream_advance([self.ch], lp_chunk[None], [int(length)], want_partial=True,
+                                     words_cap=self.words_cap)[0]
+
+    def feed(self, lp_chunk, length=None):
+        """Decode one chunk ([T_c, V] log-probs; ``length`` frames of it, all
+        by default) and return the words so far."""
+        length = int(lp_chunk.shape[0]) if length is None else int(length)
+        r = self._advance(lp_chunk, length)
+        if r["overflow"] & (OVF_ARENA | OVF_KEPT):
+            self.d.stream_release(self.ch)
+            self.prefix += list(self.last_words)
+            self.last_words = []
+            self.restarts += 1
+            self.ch = self._open()
+            r = self._advance(lp_chunk, length)
+        if r["ok"]:
+            self.last_words = list(r["words"])
+        return dict(words=self.prefix + list(r["words"]), score=r["score"], ok=r["ok"],
+                    overflow=r["overflow"], restarts=self.restarts)
+
+    def finish(self):
+        """Final step of the stream; the channel returns to the decoder."""
+        f = self.d.stream_finalize([self.ch], words_cap=self.words_cap)[0]
+        self.d.stream_release(self.ch)
+        self.ch = -1
+        words = self.prefix + (list(f["words"]) if f["ok"] else list(self.last_words))
+        return dict(words=words, score=f["score"], ok=f["ok"], reached_final=f["reached_final"],
+                    overflow=f["overflow"], restarts=self.restarts)
