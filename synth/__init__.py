@@ -302,9 +302,11 @@ def dyadic_log_probs(rng, T, V, lo=-8.0, hi=0.0, step=0.125):
 
 
 def random_tiny_graph(rng, N, V, max_deg=3, p_eps=0.0, p_final=0.5, dyadic=True,
-                      p_word=0.5, word_max=9, allow_empty=False):
+                      p_word=0.5, word_max=9, allow_empty=False, relabel=False):
     """A small random graph for brute-force checks (epsilon arcs go to higher
-    state ids only, so the epsilon subgraph is acyclic)."""
+    state ids only, so the epsilon subgraph is acyclic).  With ``relabel`` the
+    states are renamed by a random permutation afterwards (the start state
+    too), so that an epsilon-topological order no longer follows the ids."""
     src, dst, il, ol, w = [], [], [], [], []
     for s in range(N):
         deg = int(rng.integers(0 if allow_empty else 1, max_deg + 1))
@@ -329,4 +331,10 @@ def random_tiny_graph(rng, N, V, max_deg=3, p_eps=0.0, p_final=0.5, dyadic=True,
                      -np.inf).astype(np.float32)
     if not np.isfinite(final).any():
         final[int(rng.integers(0, N))] = 0.0
-    return graph_from_arcs(N, V, np.array(src, dtype=np.int64), dst, il, ol, w, final)
+    if not relabel:
+        return graph_from_arcs(N, V, np.array(src, dtype=np.int64), dst, il, ol, w, final)
+    perm = rng.permutation(N)
+    final_p = np.empty_like(final)
+    final_p[perm] = final
+    return graph_from_arcs(N, V, perm[np.array(src, dtype=np.int64)], perm[np.array(dst, dtype=np.int64)],
+                           il, ol, w, final_p, start=int(perm[0]))

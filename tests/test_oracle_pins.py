@@ -36,13 +36,16 @@ def _p(**kw):
 # ---------------------------------------------------------------- brute force
 
 @pytest.mark.parametrize("seed", range(40))
-@pytest.mark.parametrize("p_eps", [0.0, 0.35])
-def test_bruteforce_dyadic_exact_path(seed, p_eps):
+@pytest.mark.parametrize("p_eps,relabel", [(0.0, False), (0.35, False), (0.5, True)])
+def test_bruteforce_dyadic_exact_path(seed, p_eps, relabel):
+    """Relabelled graphs put epsilon arcs from higher to lower state ids, so a
+    closure that visits states in id order instead of epsilon-topological
+    order (§5.5) relaxes some state before its score is final."""
     rng = np.random.default_rng(1000 + seed)
-    N = int(rng.integers(2, 7))
+    N = int(rng.integers(2, 7)) + (3 if relabel else 0)
     V = int(rng.integers(2, 5))
     T = int(rng.integers(1, 5))
-    g = synth.random_tiny_graph(rng, N, V, max_deg=3, p_eps=p_eps, dyadic=True)
+    g = synth.random_tiny_graph(rng, N, V, max_deg=3, p_eps=p_eps, dyadic=True, relabel=relabel)
     lp = synth.dyadic_log_probs(rng, T, V)
     complete, _ = H.enumerate_paths(g, lp, T)
     G = oracle.Graph(g)
@@ -148,11 +151,16 @@ def _fan_graph():
                                  np.zeros(6, np.float32))
 
 
+def _dead_end_graph():
+    # state 0: one arc (ilabel 1) to state 1; state 1: no arcs
+    return synth.graph_from_arcs(2, 2, np.array([0]), [1], [1], [0], [0.0], np.zeros(2, np.float32))
+
+
 @pytest.mark.parametrize("case", json.load(open(os.path.join(GOLD, "beam_rule.json")))["cases"],
                          ids=lambda c: c["name"])
 def test_golden_dynamic_beam(case):
     spec = json.load(open(os.path.join(GOLD, "beam_rule.json")))
-    g = _fan_graph()
+    g = _dead_end_graph() if case.get("graph") == "dead_end" else _fan_graph()
     T = case["T"]
     lp = np.full((T, 2), -1.0, np.float32)
     p = _p(search_beam=spec["search_beam"], min_active=case["min_active"],
@@ -164,23 +172,28 @@ def test_golden_dynamic_beam(case):
     assert list(tr["n"]) == case["n"]
 
 
-def test_golden_admission_boundary():
+@pytest.mark.parametrize("case", json.load(open(os.path.join(GOLD, "admission_boundary.json")))["cases"],
+                         ids=lambda c: c["name"])
+def test_golden_admission_boundary(case):
     spec = json.load(open(os.path.join(GOLD, "admission_boundary.json")))
-    w = [0.0, -12.5, -12.375, -13.0]
-    g = synth.graph_from_arcs(5, 2, np.zeros(4, np.int64), [1, 2, 3, 4], [1] * 4, [1, 2, 3, 4], w,
-                              np.zeros(5, np.float32))
-    lp = np.full((1, 2), -0.5, np.float32)
+    src, dst, il, ol, w = (list(c) for c in zip(*case["arcs"]))
+    N = case["num_states"]
+    fin = np.zeros(N, np.float32) if case["finals"] is None else \
+        np.array([-np.inf if f is None else f for f in case["finals"]], np.float32)
+    g = synth.graph_from_arcs(N, 2, np.array(src), dst, il, ol, w, fin)
+    lp = np.full((spec["T"], 2), -0.5, np.float32)
     p = _p(search_beam=spec["search_beam"], min_active=spec["min_active"],
            max_active=spec["max_active"], lattice=True, output_beam=1e30)
-    d = oracle.Decoder(oracle.Graph(g), p, 1)
+    d = oracle.Decoder(oracle.Graph(g), p, spec["T"])
     d.advance(lp)
     tr = d.trace()
-    assert tr["max_end"][0] == np.float32(spec["max_end"])
-    assert tr["cutoff"][0] == np.float32(spec["cutoff"])
+    assert tr["max_end"][0] == np.float32(case["max_end"])
+    assert tr["cutoff"][0] == np.float32(case["cutoff"])
     r = d.finalize()
     recs = d.lattice(kept=False)
-    assert sorted(recs[recs["flags"] == 0]["dst_state"].tolist()) == spec["frame1_states"]
-    assert np.float32(r["score"]) == np.float32(spec["score"]) and list(r["words"]) == spec["words"]
+    assert sorted(recs[recs["flags"] == 0]["dst_state"].tolist()) == case["emit_states"]
+    assert sorted(recs[recs["flags"] == oracle.REC_EPS]["dst_state"].tolist()) == case["eps_states"]
+    assert np.float32(r["score"]) == np.float32(case["score"]) and list(r["words"]) == case["words"]
 
 
 # ---------------------------------------------------------------- lattice
@@ -387,6 +400,21 @@ def test_work_counters_closed_forms():
                                np.array([-np.inf, -np.inf, -np.inf, 0.0], np.float32))
     st3 = oracle.decode(oracle.Graph(g3), lp, 1, _p(search_beam=1e30))["stats"]
     assert st3["eps_relaxed"] == 4 and st3["sum_m"] == 0 and st3["finals"] == 0
+    # pruning: the first admission-boundary case (hand-derived in
+    # tests/golden/admission_boundary.json) expands n = 1 token into D = 4
+    # candidates, admits a = 2 of them into m = 2 states
+    w = [0.0, -12.5, -12.375, -13.0]
+    g4 = synth.graph_from_arcs(5, 2, np.zeros(4, np.int64), [1, 2, 3, 4], [1] * 4, [1, 2, 3, 4], w,
+                               np.zeros(5, np.float32))
+    st4 = oracle.decode(oracle.Graph(g4), np.full((1, 2), -0.5, np.float32), 1,
+                        _p(search_beam=10.0, min_active=2, max_active=100))["stats"]
+    assert (st4["sum_n"], st4["sum_D"], st4["sum_a"], st4["sum_m"]) == (1, 4, 2, 2)
+    # recombination: three admitted arcs into one state give m = 1
+    g5 = synth.graph_from_arcs(2, 2, np.zeros(3, np.int64), [1, 1, 1], [1, 1, 1], [0, 0, 0],
+                               [0.0, -1.0, -2.0], np.zeros(2, np.float32))
+    st5 = oracle.decode(oracle.Graph(g5), np.full((1, 2), -0.5, np.float32), 1,
+                        _p(search_beam=1e30))["stats"]
+    assert (st5["sum_n"], st5["sum_D"], st5["sum_a"], st5["sum_m"]) == (1, 3, 3, 1)
 
 
 def test_blank_skip_rule_by_hand():
