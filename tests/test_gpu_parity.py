@@ -29,13 +29,13 @@ def _cuda(x):
 
 # ------------------------------------------------------------ tiny random graphs
 
-def _tiny_case(seed, p_eps):
+def _tiny_case(seed, p_eps, relabel=False):
     rng = np.random.default_rng(77000 + seed)
     N = int(rng.integers(2, 40))
     V = int(rng.integers(2, 9))
     g = synth.random_tiny_graph(rng, N, V, max_deg=int(rng.integers(1, 6)), p_eps=p_eps,
                                 dyadic=bool(seed % 2 == 0), allow_empty=bool(seed % 3 == 0),
-                                p_final=float(rng.choice([0.0, 0.2, 0.6])))
+                                p_final=float(rng.choice([0.0, 0.2, 0.6])), relabel=relabel)
     B = 4
     T = int(rng.integers(1, 14))
     lens = rng.integers(0, T + 1, size=B).astype(np.int32)
@@ -60,6 +60,24 @@ def test_tiny_random_graphs(W, p_eps):
         for b in range(len(lens)):
             ref = oracle_lane(OG, lp[b], lens[b], p)
             where = f"seed {seed} eps {p_eps} lane {b}"
+            assert_lane_equal(out[b], ref, where)
+            if ref["ok"]:
+                assert_lattice_equal(D.lattice(b), ref["lattice"], where)
+        D.close()
+        G.close()
+
+
+def test_tiny_random_graphs_relabelled(W):
+    """States renamed by a random permutation: epsilon arcs also run from
+    higher to lower state ids and the start state is not state 0."""
+    for seed in range(40):
+        g, lp, lens, p = _tiny_case(seed, 0.4, relabel=True)
+        G, D = gpu_decoder(W, g, p, max_lanes=6, max_frames=lp.shape[1])
+        OG = oracle.Graph(g)
+        out = D.decode(_cuda(lp), lens)
+        for b in range(len(lens)):
+            ref = oracle_lane(OG, lp[b], lens[b], p)
+            where = f"relabelled seed {seed} lane {b}"
             assert_lane_equal(out[b], ref, where)
             if ref["ok"]:
                 assert_lattice_equal(D.lattice(b), ref["lattice"], where)
