@@ -139,8 +139,10 @@ typedef struct {
  * Upload and validate a graph on `device` (§4 "Graph Image": every index the
  * decoder follows is checked — start state, monotone row_splits, arc
  * destinations, label ranges, acyclic epsilon subgraph, finite weights).
- * On success *out owns one reference.  Errors: INVALID_ARG (NULL pointers),
- * CORRUPT_GRAPH (validation), CUDA, OOM.
+ * On success *out owns one reference.  Errors: INVALID_ARG (NULL pointers, a
+ * negative device, or a device id at or above the visible device count; the
+ * count is checked after the graph itself), CORRUPT_GRAPH (validation), CUDA
+ * (no CUDA device), OOM.
  */
 int wfst_graph_upload(const wfst_graph_desc* desc, int32_t device, wfst_graph** out);
 

@@ -79,6 +79,32 @@ def test_graph_validation_rejects_corrupt_graphs_on_host(lib):
     assert b"vocab" in lib.wfst_last_error()
 
 
+def test_graph_upload_checks_the_device_id(lib):
+    """A negative device id is refused before anything else; an id past the
+    visible devices is refused once the graph itself has validated (without
+    any CUDA device the count itself fails: WFST_ERR_CUDA)."""
+    import ctypes as C
+    import numpy as np
+    import synth
+    g = synth.graph_from_arcs(2, 2, np.array([0]), [1], [1], [0], [0.0], np.zeros(2, np.float32))
+    keep = [np.ascontiguousarray(g[k]) for k in ("row_splits", "ilabel", "olabel", "weight", "dst", "final")]
+    desc = W.GraphDesc(2, 0, 2, 0, 1, *[k.ctypes.data_as(C.c_void_p) for k in keep])
+    h = C.c_void_p()
+    assert lib.wfst_graph_upload(C.byref(desc), -1, C.byref(h)) == -1
+    assert b"device" in lib.wfst_last_error() and not h.value
+    rc = lib.wfst_graph_upload(C.byref(desc), 1 << 20, C.byref(h))
+    assert rc == (-1 if _has_cuda_device() else -3) and not h.value
+    assert b"device" in lib.wfst_last_error()
+
+
+def _has_cuda_device():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
 def test_binding_structs_match_the_header(tmp_path):
     """The ctypes mirrors of wfst_params, wfst_capacity and wfst_graph_desc
     have the header's sizes and field offsets (compiled with the host C

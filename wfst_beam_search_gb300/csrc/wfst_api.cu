@@ -93,6 +93,7 @@ extern "C" const char* wfst_last_error(void) { return g_err.c_str(); }
 extern "C" int wfst_graph_upload(const wfst_graph_desc* d, int32_t device, wfst_graph** out) {
   if (!d || !out) return fail(WFST_ERR_INVALID_ARG, "graph_upload: NULL argument");
   *out = nullptr;
+  if (device < 0) return fail(WFST_ERR_INVALID_ARG, "graph_upload: device must be >= 0");
   const int64_t N = d->num_states, A = d->num_arcs, V = d->vocab_size;
   if (N <= 0) return fail(WFST_ERR_CORRUPT_GRAPH, "corrupt graph: num_states must be positive");
   if (A < 0 || A + N >= (int64_t)INT32_MAX)
@@ -147,6 +148,15 @@ extern "C" int wfst_graph_upload(const wfst_graph_desc* d, int32_t device, wfst_
   }
 
   // internal layout: per state, emitting arcs then epsilon arcs (stable)
+  int ndev = 0;
+  const cudaError_t ce = cudaGetDeviceCount(&ndev);
+  if (ce != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(ce, "graph_upload: no CUDA device");
+  }
+  if (device >= ndev)
+    return fail(WFST_ERR_INVALID_ARG, "graph_upload: device " + std::to_string(device) + " is not among the " +
+                                          std::to_string(ndev) + " visible CUDA devices");
   std::vector<int4> meta(N);
   std::vector<uint16_t> il16(A ? A : 1);
   std::vector<float> wt(A ? A : 1);
@@ -331,6 +341,7 @@ static void decoder_destroy(wfst_decoder* d) {
     if (d->h_stats) cudaFreeHost(d->h_stats);
     if (d->h_bar) cudaFreeHost(d->h_bar);
     if (d->h_prof) cudaFreeHost(d->h_prof);
+    if (d->w.words) cudaFree(d->w.words);
     if (d->h_words) cudaFreeHost(d->h_words);
     if (d->d_stage) cudaFree(d->d_stage);
     if (d->ev0) cudaEventDestroy(d->ev0);
