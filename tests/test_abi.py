@@ -79,6 +79,27 @@ def test_graph_validation_rejects_corrupt_graphs_on_host(lib):
     assert b"vocab" in lib.wfst_last_error()
 
 
+def test_missing_library_fails_loudly():
+    """Without the built library every entry of the binding raises: there is
+    no CPU path to fall back on.  Checked in a child process that points the
+    binding at a library file that does not exist."""
+    import sys
+    code = (
+        "import numpy as np, synth, wfst_beam_search_gb300 as W\n"
+        "from wfst_beam_search_gb300 import _build\n"
+        "_build.LIB = '/nonexistent/libwfst_gb300.so'\n"
+        "for f in (W.load, lambda: W.Graph(synth.make_graph(0), device=0)):\n"
+        "    try:\n"
+        "        f()\n"
+        "    except ImportError as e:\n"
+        "        assert 'no CPU fallback' in str(e), e\n"
+        "    else:\n"
+        "        raise SystemExit('no error')\n"
+        "print('ok')\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stderr[-2000:]
+
+
 def test_graph_upload_checks_the_device_id(lib):
     """A negative device id is refused before anything else; an id past the
     visible devices is refused once the graph itself has validated (without
