@@ -100,6 +100,21 @@ def test_missing_library_fails_loudly():
     assert r.returncode == 0 and r.stdout.strip() == "ok", r.stderr[-2000:]
 
 
+def test_log_prob_arguments_are_checked_on_the_host():
+    import numpy as np
+    with pytest.raises(ValueError, match=r"\[B, T, V\]"):
+        W._lp_args(np.zeros((4, 5), np.float32))
+    with pytest.raises(TypeError):
+        W._lp_args(np.zeros((1, 4, 5), np.float64))
+    with pytest.raises(ValueError, match="unit stride"):
+        W._lp_args(np.zeros((1, 5, 4), np.float32).transpose(0, 2, 1))
+    lp = np.zeros((2, 3, 5), np.float16)[:, ::2]
+    _, dt, sb, st, B, T = W._lp_args(lp)
+    assert (dt, sb, st, B, T) == (W.WFST_F16, 15, 10, 2, 2)
+    # host arrays keep the caller's stream choice (None: the default stream)
+    assert W._default_stream(lp, None) is None and W._default_stream(lp, 7) == 7
+
+
 def test_graph_upload_checks_the_device_id(lib):
     """A negative device id is refused before anything else; an id past the
     visible devices is refused once the graph itself has validated (without

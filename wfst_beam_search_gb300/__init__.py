@@ -309,6 +309,8 @@ def make_params(search_beam=20.0, output_beam=8.0, min_active=30, max_active=100
 
 def _lp_args(lp):
     """(pointer, dtype code, stride_b, stride_t, B, T) of a [B, T, V] tensor."""
+    if len(lp.shape) != 3:
+        raise ValueError(f"log_probs must be [B, T, V], got shape {tuple(lp.shape)}")
     if isinstance(lp, np.ndarray):
         if lp.dtype not in (np.float32, np.float16):
             raise TypeError("log_probs must be float32 or float16")
@@ -347,7 +349,10 @@ class Decoder:
             pass
 
     def decode(self, lp, lens, stream=None, words_cap=4096):
-        """Offline decode of [B, T, V] log-probs (torch CUDA tensor or numpy)."""
+        """Offline decode of [B, T, V] log-probs (torch CUDA tensor or numpy).
+        The call runs on ``stream``; by default, for a CUDA tensor, on torch's
+        current stream of its device (where its producer most likely ran)."""
+        stream = _default_stream(lp, stream)
         ptr, dt, sb, st, B, T = _lp_args(lp)
         lens = np.ascontiguousarray(lens, dtype=np.int32)
         words = np.zeros((B, max(words_cap, 1)), np.int32)
@@ -381,6 +386,7 @@ class Decoder:
                        words_cap=4096):
         ch = np.ascontiguousarray(channels, dtype=np.int32)
         n = len(ch)
+        stream = _default_stream(lp, stream)
         ptr, dt, sb, st, B, T = _lp_args(lp)
         if B != n:
             raise ValueError("one log-prob row per channel")
@@ -413,6 +419,15 @@ class Decoder:
 
     def stream_release(self, channel: int):
         wfst_stream_release(self.h, int(channel))
+
+
+def _default_stream(lp, stream):
+    """The stream a call on ``lp`` runs on when the caller names none: torch's
+    current stream of a CUDA tensor's device, else the default stream."""
+    if stream is not None or isinstance(lp, np.ndarray) or not getattr(lp, "is_cuda", False):
+        return stream
+    import torch
+    return torch.cuda.current_stream(lp.device)
 
 
 def _stream(s):
