@@ -218,7 +218,8 @@ int wfst_stream_create(wfst_decoder* d, int32_t* channel);
  * or host, strides as in wfst_decode), chunk_lens host [n] in [0, chunk_T].
  * Online beam semantics: the offline last-frames rule never fires (§3).
  * If want_partial, the outputs receive each channel's best current
- * hypothesis (§8: from the best current-frontier token), laid out as in
+ * hypothesis (§8: backtracked from the highest-scoring token of the
+ * channel's current frontier), laid out as in
  * wfst_decode (meta reached_final is 0); otherwise they may be NULL.
  */
 int wfst_stream_advance(wfst_decoder* d, const int32_t* channels, int32_t n,
@@ -310,8 +311,8 @@ int wfst_decode_static(const wfst_graph* g, const wfst_params* params, const voi
 
 /*
  * Blank-skip frame pre-slicing, a pre-pass outside the decoder (§3 Decoding
- * Semantics: "blank-skip stays outside the decoder", WeNet-style, threshold
- * 0.98 by default).  Frame t < lens[b] of lane b is dropped iff
+ * Semantics: blank-dominated frames are removed before the search, not
+ * inside it, WeNet-style, threshold 0.98 by default).  Frame t < lens[b] of lane b is dropped iff
  * log_probs[b, t, blank_id] > log(threshold), with log(threshold) computed in
  * double and rounded once to fp32 and the log-prob widened exactly to fp32.
  * The kept rows are packed in order into out[b, i, v] at out + (b*T + i)*V

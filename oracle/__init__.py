@@ -240,8 +240,9 @@ def decode_batch(graph: Graph, lp, lens, p: dict, threads: int = 1, lattice_out=
 
 def blank_skip(lp, lens, threshold=0.98, blank=0):
     """Blank-skip frame pre-slicing, outside the decoder (page "GPU WFST
-    Beam-Search Decoder", §3 Decoding Semantics: blank-skip stays outside the
-    decoder, WeNet-style frame pre-slicing, threshold 0.98 by default).
+    Beam-Search Decoder", §3 Decoding Semantics: blank-dominated frames are
+    removed before the search, in the WeNet manner, threshold 0.98 by
+    default).
 
     Frame t < lens[b] of lane b is dropped when its blank posterior is above
     the threshold, tested in the log domain in fp32: lp[b, t, blank] (widened

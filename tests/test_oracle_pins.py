@@ -418,9 +418,9 @@ def test_work_counters_closed_forms():
 
 
 def test_blank_skip_rule_by_hand():
-    """Blank-skip pre-slicing (§3: blank-skip stays outside the decoder,
-    WeNet-style, threshold 0.98): a frame is dropped when its blank posterior
-    is above the threshold.  Expected frames written out from the posteriors."""
+    """Blank-skip pre-slicing (§3: blank-dominated frames are removed before
+    the search, WeNet-style, threshold 0.98): a frame is dropped when its
+    blank posterior is above the threshold.  Expected frames written out from the posteriors."""
     import oracle
     thr = 0.98
     lthr = np.float32(np.log(0.98))

@@ -1,8 +1,8 @@
 """The caller-side overflow policy of StreamingSearch (page "GPU WFST
 Beam-Search Decoder", §7 overflow handling and §8.1): a chunk that comes
 back flagged abandons its channel, keeps the hypothesis from before that
-chunk as a prefix and decodes the chunk again on a fresh channel.  Checked on
-the CPU against a scripted stand-in for the streaming decoder calls."""
+chunk as a prefix and runs the chunk once more on a newly opened channel.
+Checked on the CPU against a scripted stand-in for the streaming decoder calls."""
 import numpy as np
 
 import wfst_beam_search_gb300 as W

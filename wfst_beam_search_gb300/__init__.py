@@ -445,8 +445,9 @@ class StreamingSearch:
     with a capacity overflow bit set (winners log or frontier: the channel's
     search state is incomplete) cannot be trusted from then on, so it is
     abandoned, the hypothesis it gave before that chunk is kept as a finished
-    prefix, and the chunk is decoded again on a fresh channel.  The search
-    context across the burst is lost; the audio after it is not.
+    prefix, and the chunk runs once more on a newly opened channel.  The new
+    channel starts its search from scratch, so hypotheses that spanned the
+    overflow are gone, but no frame after it is skipped.
 
     ``feed`` returns the words so far (prefix + the channel's partial
     hypothesis); ``finish`` runs the final step and releases the channel.

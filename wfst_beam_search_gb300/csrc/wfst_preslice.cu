@@ -1,8 +1,9 @@
 // wfst_preslice.cu — blank-skip frame pre-slicing, a pre-pass outside the
-// decoder ("GPU WFST Beam-Search Decoder", §3 Decoding Semantics: blank-skip
-// stays outside the decoder, WeNet-style frame pre-slicing with threshold
-// 0.98 by default; skipping inside the search would be wrong on graphs whose
-// states do not all carry a blank self-loop).
+// decoder ("GPU WFST Beam-Search Decoder", §3 Decoding Semantics: frames
+// whose blank posterior passes a threshold, 0.98 by default, are removed
+// before the search, in the WeNet manner, not inside it; skipping inside the
+// search would be wrong on graphs whose states do not all carry a blank
+// self-loop).
 //
 // A frame t < lens[b] of lane b is dropped iff its blank log-posterior is
 // above log(threshold): lp[b, t, blank] > lthr, where lthr is log(threshold)
