@@ -40,6 +40,7 @@ import synth  # noqa: E402
 # weight (6 B), an admitted candidate's destination and recombination entry
 # (16 B), a new token's record, winners-log entry and cleared entry (32 B).
 BYTES_N, BYTES_D, BYTES_A, BYTES_M = 20, 6, 16, 32
+L2_MB = 129   # GB300 L2 capacity
 
 
 # DRAM bytes (read + write) of one decode launch of this bench's default
@@ -172,50 +173,88 @@ def workload_name(wl):
     return f"{wl.name}-B{wl.B}xT{wl.T}xV{wl.V}-{wl.dtype}"
 
 
-def cpu_baseline(wi, seconds_target=20.0, threads=None):
-    """The oracle as it stands, on the host cores, over a bounded sample of
-    lanes of the same workload (one lane per thread)."""
+def workload_config(wl, g, lanes_per_rank, ws, gc_interval):
+    """The `config` object of both arms' JSON lines."""
+    # device bytes of the decoder's graph layout: 20 per state (row data,
+    # final weight) and 28 per arc (the 16-byte record, source, destination
+    # and output label columns)
+    lp_mb = lanes_per_rank * wl.T * wl.V * (2 if wl.dtype == "f16" else 4) / 1e6
+    graph_mb = (20 * g["num_states"] + 28 * g["num_arcs"]) / 1e6
+    big = lp_mb + graph_mb > L2_MB
+    l2 = (f"inputs {'larger than' if big else 'within'} L2 ({L2_MB} MB): {lp_mb:.0f} MB log-probs per rank, "
+          f"{graph_mb:.0f} MB graph; no flush" + ("" if big else " (a small case, L2-resident)"))
+    return {"workload": workload_name(wl), "graph": f"{g['num_states']} states / {g['num_arcs']} arcs",
+            "global_batch": lanes_per_rank * ws, "frames_per_utt": wl.T, "vocab": wl.V,
+            "log_probs": wl.dtype, "search_beam": wl.search_beam, "max_active": wl.max_active,
+            "min_active": wl.min_active, "parallelism": f"replicas x{ws} (lanes sharded)",
+            "l2": l2,
+            "mode": (f"streaming: {wl.chunk}-frame chunks, partial per chunk, finalize with lattice"
+                     if wl.streaming else "offline"),
+            "gc_interval": gc_interval}
+
+
+def oracle_sample(wi, threads=None):
+    """The oracle's inputs for a bounded sample of lanes of workload `wi`:
+    one lane per host thread (at most the workload's B lanes)."""
     import oracle
     wl = synth.workload(wi)
     threads = threads or os.cpu_count() or 1
     g = synth.make_graph(wi)
-    OG = oracle.Graph(g)
-    p = oracle.params(wl.search_beam, wl.output_beam, wl.min_active, wl.max_active, True, False)
     lanes = list(range(min(threads, wl.B)))
-    lp = synth.make_log_probs(wi, lanes=lanes)
-    lens = synth.make_lens(wi)[lanes]
+    return {"wl": wl, "g": g, "OG": oracle.Graph(g), "lanes": lanes,
+            "p": oracle.params(wl.search_beam, wl.output_beam, wl.min_active, wl.max_active, True, False),
+            "lp": synth.make_log_probs(wi, lanes=lanes), "lens": synth.make_lens(wi)[lanes]}
+
+
+def oracle_run(s):
+    """One timed pass of the oracle over the sample: (seconds, frames, arcs expanded)."""
+    import oracle
     t0 = time.perf_counter()
-    res = oracle.decode_batch(OG, lp, lens, p, threads=len(lanes))
+    res = oracle.decode_batch(s["OG"], s["lp"], s["lens"], s["p"], threads=len(s["lanes"]))
     dt = time.perf_counter() - t0
-    frames = int(sum(lens))
-    arcs = int(sum(r["stats"]["arcs_expanded"] for r in res))
-    return {"value": frames / dt, "unit": "frames/s", "cores": len(lanes), "kind": "oracle",
-            "sample": f"{len(lanes)} of {wl.B} lanes of workload '{wl.name}' ({frames} frames), one lane per thread",
-            "arcs_per_s": arcs / dt, "seconds": dt}
+    return dt, int(sum(s["lens"])), int(sum(r["stats"]["arcs_expanded"] for r in res))
+
+
+def sample_text(s):
+    wl = s["wl"]
+    return (f"{len(s['lanes'])} of {wl.B} lanes of workload '{wl.name}' ({int(sum(s['lens']))} frames), "
+            f"one lane per thread")
+
+
+def cpu_baseline(wi, threads=None):
+    """The oracle as it stands, on the host cores, over a bounded sample of
+    lanes of the same workload (one lane per thread)."""
+    s = oracle_sample(wi, threads)
+    dt, frames, arcs = oracle_run(s)
+    return {"value": frames / dt, "unit": "frames/s", "cores": len(s["lanes"]), "kind": "oracle",
+            "sample": sample_text(s), "arcs_per_s": arcs / dt, "seconds": dt}
 
 
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    wl = synth.workload(args.workload)
-    import oracle  # noqa: F401
+    # the sample (graph, inputs) is built once; each step is one timed pass
+    s = oracle_sample(args.workload)
+    wl = s["wl"]
     times, frames_tot, arcs_tot = [], 0, 0
-    cb = None
     for i in range(args.warmup + args.steps):
-        cb = cpu_baseline(args.workload)
+        dt, frames, arcs = oracle_run(s)
         if i >= args.warmup:
-            times.append(cb["seconds"])
-    value = cb["value"]
+            times.append(dt)
+            frames_tot += frames
+            arcs_tot += arcs
+    value = frames_tot / sum(times)
+    cores = len(s["lanes"])
     line = {
         "impl": "reference", "metric": "frames/s", "value": value, "unit": "frames/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": workload_name(wl), "lanes_per_step": cb["cores"]},
-        "arcs_expanded_per_s": cb["arcs_per_s"],
-        "cpu_baseline": {"value": value, "unit": "frames/s", "cores": cb["cores"], "kind": "oracle",
-                         "sample": cb["sample"]},
+        "config": workload_config(wl, s["g"], args.lanes or wl.B, args.gpus, args.gc_interval),
+        "arcs_expanded_per_s": arcs_tot / sum(times),
+        "cpu_baseline": {"value": value, "unit": "frames/s", "cores": cores, "kind": "oracle",
+                         "sample": sample_text(s) + f", {args.steps} timed passes"},
         "e2e": {"value": value, "unit": "frames/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -348,14 +387,7 @@ def run_gpu(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": workload_name(wl), "graph": f"{g['num_states']} states / {g['num_arcs']} arcs",
-                   "global_batch": B * ws, "frames_per_utt": T, "vocab": wl.V, "log_probs": wl.dtype,
-                   "search_beam": wl.search_beam, "max_active": wl.max_active,
-                   "min_active": wl.min_active, "parallelism": f"replicas x{ws} (lanes sharded)",
-                   "l2": "inputs larger than L2 (320 MB log-probs, 320 MB graph, ~15 GB workspace); no flush",
-                   "mode": (f"streaming: {wl.chunk}-frame chunks, partial per chunk, finalize with lattice"
-                            if wl.streaming else "offline"),
-                   "gc_interval": args.gc_interval},
+        "config": workload_config(wl, g, B, ws, args.gc_interval),
         "arcs_expanded_per_s": arcs_per_s,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": measured_traffic(workload_name(wl), B),
@@ -396,6 +428,8 @@ def main():
     ap.add_argument("--gc-interval", type=int, default=0,
                     help="winners-log GC every N frames per lane (0: off; turns the lattice off)")
     args = ap.parse_args()
+    if args.steps < 1 or args.warmup < 0:
+        ap.error("--steps must be >= 1 and --warmup >= 0")
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)
