@@ -196,6 +196,50 @@ def test_golden_admission_boundary(case):
     assert np.float32(r["score"]) == np.float32(case["score"]) and list(r["words"]) == case["words"]
 
 
+_NONMONO = json.load(open(os.path.join(GOLD, "beam_not_monotone.json")))
+
+
+@pytest.mark.parametrize("case", _NONMONO["cases"], ids=lambda c: f"beam {c['search_beam']:g}")
+def test_golden_best_score_is_not_monotone_in_the_beam(case):
+    """A wider beam admits a branch whose higher maximum at the next step
+    prunes the prefix of the narrower search's best path: beam 1 gives -5.5,
+    beam 2 gives -13, an unbounded beam -5.5 again (hand-derived in the
+    fixture).  A search that pruned against a per-token or stale maximum
+    would not reproduce it."""
+    spec = _NONMONO
+    src, dst, il, ol, w = (list(c) for c in zip(*spec["arcs"]))
+    N = spec["num_states"]
+    fin = np.array([-np.inf if f is None else f for f in spec["finals"]], np.float32)
+    g = synth.graph_from_arcs(N, 2, np.array(src), dst, il, ol, w, fin)
+    p = _p(search_beam=case["search_beam"], min_active=spec["min_active"],
+           max_active=spec["max_active"], allow_partial=False)
+    d = oracle.Decoder(oracle.Graph(g), p, None)
+    d.advance(np.full((spec["T"], 2), -0.5, np.float32))
+    r = d.finalize()
+    assert r["ok"] == 1 and r["reached_final"] == case["reached_final"]
+    assert np.float32(r["score"]) == np.float32(case["score"])
+    assert list(r["words"]) == case["words"]
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_pruned_search_never_beats_the_unpruned_optimum(seed):
+    """What does hold for every beam: a pruned search returns a real path, so
+    its score is at most the unpruned optimum, and if it reaches a final
+    state so does the unpruned search.  (The best score is not monotone in
+    the beam; see the golden case above.)"""
+    rng = np.random.default_rng(9000 + seed)
+    N, V, T = int(rng.integers(3, 30)), int(rng.integers(2, 6)), int(rng.integers(2, 12))
+    g = synth.random_tiny_graph(rng, N, V, max_deg=4, p_eps=0.3 if seed % 2 else 0.0, dyadic=False)
+    lp = np.log(rng.dirichlet(np.ones(V), size=T)).astype(np.float32)
+    OG = oracle.Graph(g)
+    best = oracle.decode(OG, lp, T, _p(**H.INF_BEAM, allow_partial=False))
+    for beam in (0.5, 1.0, 2.0, 4.0, 8.0):
+        r = oracle.decode(OG, lp, T, _p(search_beam=beam, min_active=0, max_active=2**31 - 1,
+                                        allow_partial=False))
+        if r["ok"]:
+            assert best["ok"] == 1 and r["score"] <= best["score"], (beam, r["score"], best["score"])
+
+
 # ---------------------------------------------------------------- lattice
 
 @pytest.mark.parametrize("seed", range(30))
