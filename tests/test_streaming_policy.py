@@ -4,6 +4,7 @@ back flagged abandons its channel, keeps the hypothesis from before that
 chunk as a prefix and runs the chunk once more on a newly opened channel.
 Checked on the CPU against a scripted stand-in for the streaming decoder calls."""
 import numpy as np
+import pytest
 
 import wfst_beam_search_gb300 as W
 
@@ -12,8 +13,12 @@ class ScriptedDecoder:
     """Channels that emit one word per chunk (the chunk's first value); a
     channel overflows on the chunks listed in `burst` of its own life."""
 
-    def __init__(self, burst=(), n_channels=2):
-        self.burst = set(burst)
+    def __init__(self, burst=(), n_channels=2, bits=None, final_ok=1):
+        # burst: chunk numbers (of a channel's own life) on which channel 0
+        # overflows, or {channel: chunk numbers}
+        self.burst = {c: set(v) for c, v in burst.items()} if isinstance(burst, dict) else {0: set(burst)}
+        self.bits = W.OVF_KEPT if bits is None else bits
+        self.final_ok = final_ok
         self.free = list(range(n_channels))
         self.open = {}
         self.log = []
@@ -36,7 +41,7 @@ class ScriptedDecoder:
         st = self.open[ch]
         st["chunks"] += 1
         st["words"].append(int(lp[0][0][0]))
-        ovf = W.OVF_KEPT if (st["chunks"] in self.burst and ch == 0) else 0
+        ovf = self.bits if st["chunks"] in self.burst.get(ch, ()) else 0
         self.log.append(("advance", ch, int(lp[0][0][0])))
         return [dict(words=np.array(st["words"], np.int32), score=-float(len(st["words"])), ok=1,
                      overflow=ovf)]
@@ -44,8 +49,8 @@ class ScriptedDecoder:
     def stream_finalize(self, chans, words_cap=4096):
         (ch,) = chans
         st = self.open[ch]
-        return [dict(words=np.array(st["words"], np.int32), score=-1.0, ok=1, reached_final=1,
-                     overflow=0)]
+        return [dict(words=np.array(st["words"] if self.final_ok else [], np.int32), score=-1.0,
+                     ok=self.final_ok, reached_final=self.final_ok, overflow=0)]
 
 
 def _chunk(word):
@@ -78,3 +83,45 @@ def test_overflowed_chunk_is_decoded_again_on_a_fresh_channel():
     assert ("release", 0) in d.log and ("advance", 1, 23) in d.log
     assert d.log.index(("release", 0)) < d.log.index(("advance", 1, 23))
     assert sorted(d.free) == [0, 1]
+
+
+def test_path_overflow_is_reported_without_a_restart():
+    """Bit 32 (best path longer than the path buffer) is only reported: a new
+    channel would have no larger buffer."""
+    d = ScriptedDecoder(burst={2}, bits=W.OVF_PATH)
+    s = W.StreamingSearch(d)
+    outs = [s.feed(_chunk(w)) for w in (31, 32, 33)]
+    assert outs[1]["overflow"] == W.OVF_PATH and outs[1]["restarts"] == 0
+    assert s.finish()["words"] == [31, 32, 33]
+    assert [e for e in d.log if e[0] == "create"] == [("create", 0)]
+
+
+def test_a_retried_chunk_that_overflows_again_is_reported_and_not_kept():
+    """Channel 0 overflows on chunk 2; its retry on channel 1 overflows too
+    (channel 1 overflows on its first and second chunks).  The flagged retry
+    is reported, and its words never become part of the finished prefix."""
+    d = ScriptedDecoder(burst={0: {2}, 1: {1, 2}}, n_channels=3)
+    s = W.StreamingSearch(d)
+    r1 = s.feed(_chunk(41))
+    r2 = s.feed(_chunk(42))
+    assert r1["words"] == [41]
+    assert r2["restarts"] == 1 and r2["overflow"] == W.OVF_KEPT and r2["words"] == [41, 42]
+    # chunk 3 overflows channel 1 again: the restart on channel 2 keeps the
+    # prefix [41] only (never the flagged [42])
+    r3 = s.feed(_chunk(43))
+    assert r3["restarts"] == 2 and r3["overflow"] == 0 and r3["words"] == [41, 43]
+
+
+def test_failed_final_step_falls_back_to_the_last_partial():
+    d = ScriptedDecoder(final_ok=0)
+    s = W.StreamingSearch(d)
+    for w in (51, 52):
+        s.feed(_chunk(w))
+    f = s.finish()
+    assert f["ok"] == 0 and f["words"] == [51, 52]
+
+
+def test_no_free_channel_raises():
+    d = ScriptedDecoder(n_channels=0)
+    with pytest.raises(RuntimeError, match="busy"):
+        W.StreamingSearch(d)

@@ -483,7 +483,9 @@ class StreamingSearch:
             self.restarts += 1
             self.ch = self._open()
             r = self._advance(lp_chunk, length)
-        if r["ok"]:
+        # only a result whose search state is complete may later become the
+        # finished prefix (a retried chunk can overflow again: it is reported)
+        if r["ok"] and not (r["overflow"] & (OVF_ARENA | OVF_KEPT)):
             self.last_words = list(r["words"])
         return dict(words=self.prefix + list(r["words"]), score=r["score"], ok=r["ok"],
                     overflow=r["overflow"], restarts=self.restarts)
