@@ -21,7 +21,8 @@
  *     caller.
  *   - A lane whose capacity was exceeded is not an error: its meta[2]
  *     overflow bits are set (§7 "Overflow bits") and its result may be
- *     degraded; re-run it with larger capacities (decoding is idempotent).
+ *     degraded.  Offline decodes grow the capacity and re-run such lanes
+ *     themselves (see wfst_decode); streaming channels only report it.
  *   - Exact-score ties are broken by the LOWEST arc id (final-state ties by
  *     the lowest state), so results are deterministic and bit-exact with the
  *     CPU reference.  (§3 leaves ties to atomic scheduling.)
@@ -106,8 +107,9 @@ typedef struct {
 typedef struct {
   int64_t frontier_cap;   /* tokens per lane per frame (default: num_states, never overflows) */
   int64_t log_cap;        /* winners-log entries per lane (default (max_frames+2)*4*max_active, >= 1Mi) */
-  int64_t lattice_cap;    /* lattice records per lane (default (max_frames+2)*2*max_active) */
-  int64_t path_cap;       /* arcs of one best path (default 4*(max_frames+2)) */
+  int64_t lattice_cap;    /* lattice records per lane (default (max_frames+2)*2*max_active, >= 1Mi) */
+  int64_t path_cap;       /* arcs of one best path (default 4*(max_frames+2)*(1 + epsilon depth);
+                             with the GC, 4*max(max_frames+2, 1024)*(1 + epsilon depth)) */
   int64_t fin_cap;        /* GC only: finalized words per lane (default 65536) */
 } wfst_capacity;
 
@@ -188,7 +190,8 @@ void wfst_decoder_free(wfst_decoder* d);
  * created with WFST_OPT_NO_GROW.  Decoding is idempotent, so the re-run
  * lanes give the results an unbounded decoder would give.
  * The call is stream-ordered on `stream` and returns after the results are
- * on the host.  Errors: INVALID_ARG, STATE, CUDA, TIMEOUT, OOM.
+ * on the host.  Errors: INVALID_ARG, STATE (a streaming decoder), CAPACITY
+ * (T too large for the frame tables), CUDA, TIMEOUT, OOM.
  */
 int wfst_decode(wfst_decoder* d, const void* log_probs, int32_t dtype, int64_t stride_b,
                 int64_t stride_t, const int32_t* lens, int32_t B, int32_t T, void* stream,
@@ -210,7 +213,8 @@ int wfst_lattice_export(wfst_decoder* d, int32_t lane, wfst_lat_record* out, int
 /* ---- streaming (§8 "Streaming Lifecycle"); decoder created with streaming = 1 */
 
 /* Claim a free channel (= lane) and open its start frontier; *channel = -1
- * when every channel is busy. */
+ * (and WFST_OK) when every channel is busy.  Errors: INVALID_ARG, STATE (not
+ * a streaming decoder), CUDA, TIMEOUT. */
 int wfst_stream_create(wfst_decoder* d, int32_t* channel);
 
 /*
@@ -219,8 +223,14 @@ int wfst_stream_create(wfst_decoder* d, int32_t* channel);
  * Online beam semantics: the offline last-frames rule never fires (§3).
  * If want_partial, the outputs receive each channel's best current
  * hypothesis (§8: backtracked from the highest-scoring token of the
- * channel's current frontier), laid out as in
- * wfst_decode (meta reached_final is 0); otherwise they may be NULL.
+ * channel's current frontier), laid out as in wfst_decode (meta
+ * reached_final is 0); otherwise they may be NULL.  Channels do not grow
+ * their capacities mid-stream: an overflow is reported in meta (a caller can
+ * restart the stream on a fresh channel, as the binding's StreamingSearch
+ * does).  Errors: INVALID_ARG (channel ids out of range or repeated,
+ * chunk_T > max_frames, lengths, strides, a lattice stream longer than
+ * max_frames), STATE (not a streaming decoder, a channel not open), CUDA,
+ * TIMEOUT.
  */
 int wfst_stream_advance(wfst_decoder* d, const int32_t* channels, int32_t n,
                         const void* log_probs, int32_t dtype, int64_t stride_b, int64_t stride_t,
@@ -229,17 +239,21 @@ int wfst_stream_advance(wfst_decoder* d, const int32_t* channels, int32_t n,
                         double* scores, int32_t* meta);
 
 /* Final step + backtrack (+ lattice prune) of n channels; outputs as in
- * wfst_decode.  The channels stay claimed until wfst_stream_release. */
+ * wfst_decode.  The channels stay claimed until wfst_stream_release.
+ * Errors: INVALID_ARG, STATE (not a streaming decoder, a channel not open),
+ * CUDA, TIMEOUT. */
 int wfst_stream_finalize(wfst_decoder* d, const int32_t* channels, int32_t n, void* stream,
                          int32_t* words, int32_t words_cap, int32_t* word_lens, double* scores,
                          int32_t* meta);
 
-/* Return a channel to the pool (its lattice is discarded). */
+/* Return a channel to the pool (its lattice is discarded).  Errors:
+ * INVALID_ARG (channel not in use), CUDA. */
 int wfst_stream_release(wfst_decoder* d, int32_t channel);
 
 /*
  * Counters of the last decode / stream call (host int64, n entries written,
- * at most WFST_STAT_COUNT): see WFST_STAT_* for the order.
+ * at most WFST_STAT_COUNT): see WFST_STAT_* for the order.  Errors:
+ * INVALID_ARG (NULL pointers, n < 0).
  */
 #define WFST_STAT_FRAMES 0        /* frames consumed (sum over lanes) */
 #define WFST_STAT_ARCS 1          /* arcs expanded: emitting + epsilon relaxations + final arcs */
@@ -270,6 +284,7 @@ int wfst_stats(wfst_decoder* d, int64_t* out, int32_t n);
  * the number of capacity doublings so far, then max_frames (which offline
  * decodes of longer utterances raise).  §6.2 of the page reports the
  * decoder's memory the same way; here capacities only grow on demand.
+ * Errors: INVALID_ARG (NULL pointers, n < 0).
  */
 #define WFST_MEM_BYTES 0
 #define WFST_MEM_FRONTIER_CAP 1
@@ -284,9 +299,9 @@ int wfst_mem_stats(wfst_decoder* d, int64_t* out, int32_t n);
 /*
  * Offline decode that allocates nothing (no device or pinned memory, no
  * decoder object).  "GPU WFST Beam-Search Decoder" has no counterpart: its
- * decoder sizes a workspace per decoder (§6.1).  This is the same decode as wfst_decode for
- * callers that may not allocate once running (their own memory pool, a
- * real-time thread): its working memory is one region of
+ * decoder sizes a workspace per decoder (§6.1).  This is the same decode
+ * as wfst_decode for callers that may not allocate once running (their own
+ * memory pool, a real-time thread): its working memory is one region of
  * WFST_STATIC_SCRATCH_BYTES that the library declares statically, one per
  * device per process.
  * Arguments as in wfst_decode, with the decoder replaced by the graph and
@@ -312,8 +327,8 @@ int wfst_decode_static(const wfst_graph* g, const wfst_params* params, const voi
 /*
  * Blank-skip frame pre-slicing, a pre-pass outside the decoder (§3 Decoding
  * Semantics: blank-dominated frames are removed before the search, not
- * inside it, WeNet-style, threshold 0.98 by default).  Frame t < lens[b] of lane b is dropped iff
- * log_probs[b, t, blank_id] > log(threshold), with log(threshold) computed in
+ * inside it, WeNet-style, threshold 0.98 by default).  Frame t < lens[b] of
+ * lane b is dropped iff log_probs[b, t, blank_id] > log(threshold), with log(threshold) computed in
  * double and rounded once to fp32 and the log-prob widened exactly to fp32.
  * The kept rows are packed in order into out[b, i, v] at out + (b*T + i)*V
  * (same dtype), out_lens[b] receives the kept count and frame_map[b*T + i] the
