@@ -54,6 +54,20 @@ def test_last_error_and_argument_checks_without_gpu(lib):
     assert lib.wfst_decode(None, None, 0, 0, 0, None, 0, 0, None, None, 0, None, None, None) == -1
     assert lib.wfst_decode_static(None, None, None, 0, 0, 0, None, 0, 0, None, None, 0, None, None,
                                   None) == -1
+    import ctypes as C
+    n = C.c_int64()
+    ch = C.c_int32()
+    for rc in (lib.wfst_lattice_export(None, 0, None, 0, C.byref(n)),
+               lib.wfst_stream_create(None, C.byref(ch)),
+               lib.wfst_stream_advance(None, None, 0, None, 0, 0, 0, None, 0, 0, None, None, 0, None,
+                                       None, None),
+               lib.wfst_stream_finalize(None, None, 0, None, None, 0, None, None, None),
+               lib.wfst_stream_release(None, 0),
+               lib.wfst_stats(None, None, 0),
+               lib.wfst_mem_stats(None, None, 0),
+               lib.wfst_decoder_create(None, None, 1, 1, None, None)):
+        assert rc == -1
+        assert lib.wfst_last_error()
 
 
 def test_graph_validation_rejects_corrupt_graphs_on_host(lib):
