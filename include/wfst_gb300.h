@@ -172,7 +172,10 @@ void wfst_decoder_free(wfst_decoder* d);
  * Offline batched decode (§1, §3, §7).  log_probs: [B, T, V] elements of
  * `dtype`, element (b, t, v) at log_probs[b*stride_b + t*stride_t + v]
  * (unit stride over v, stride_t >= V).  It may be a device pointer (read in
- * place) or a host pointer (copied to device inside the call).  lens: host
+ * place) or a host pointer (copied to device inside the call).  Entries are
+ * log-posteriors: finite or -INFINITY (a label that cannot be emitted); NaN
+ * and +INFINITY are outside the contract and not checked (the input is read
+ * in place, once).  lens: host
  * [B], 0 <= lens[b] <= T.  Requires B <= max_lanes and a decoder created with
  * streaming = 0.  T above max_frames first grows the decoder's per-frame
  * tables to max(T, 2 * max_frames) (§6 frame-capacity doubling; the
