@@ -79,3 +79,7 @@ def test_reference_arm_rank_zero_prints_one_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["metric"] == "frames/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+    # the same config object as the GPU arm's line (2 ranks x the workload's lanes)
+    import synth
+    wl = synth.workload(0)
+    assert d["config"] == bench.workload_config(wl, synth.make_graph(0), wl.B, 2, 0)
