@@ -30,7 +30,9 @@
  *     integer max_active / 2.
  *   - the beam update uses the current frontier size, before this step's
  *     cutoff; relax on the closed interval [min_active, max_active] or an
- *     empty frontier.  All arithmetic is IEEE fp32, round to nearest, no
+ *     empty frontier.  Its constants follow the page's text and are pinned to
+ *     hand-derived values of that text; against k2's own implementation,
+ *     which is not available here: parity unpinned.  All arithmetic is IEEE fp32, round to nearest, no
  *     fused multiply-add (compile with -ffp-contract=off).
  *   - epsilon closure: a full closure in epsilon-topological order (ties by
  *     lower state id), each relaxation admitted iff e > the emitting step's
