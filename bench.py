@@ -403,6 +403,7 @@ def run_gpu(args):
         "steps_per_decode": st0["steps"], "barriers_per_decode": st0["barriers"],
         "gpu_launches": args.steps * calls_per_step,
         "lanes_ok": res_ok,
+        "lanes_overflowed": int((meta[:, 2] != 0).sum()),   # capacity bits left after growth (0 expected)
         "clocks": clk,
         "cpu_baseline": cpu,
     }
