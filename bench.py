@@ -40,7 +40,45 @@ import synth  # noqa: E402
 # weight (6 B), an admitted candidate's destination and recombination entry
 # (16 B), a new token's record, winners-log entry and cleared entry (32 B).
 BYTES_N, BYTES_D, BYTES_A, BYTES_M = 20, 6, 16, 32
-L2_MB = 129   # GB300 L2 capacity
+# `dtype` of both arms' lines: the arithmetic of the path (fp32 sums of
+# score, weight and log-prob); the log-probs are read as config.log_probs
+# and widened exactly.
+DTYPE, DTYPE_NOTE = "f32", "arithmetic: fp32 sums; log-probs read in config.log_probs, widened exactly"
+
+
+def l2_bytes():
+    """L2 capacity of the current CUDA device as the runtime reports it
+    (cudaDevAttrL2CacheSize), or None without a device."""
+    try:
+        import torch
+        if torch.cuda.is_available():
+            return int(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+    except Exception:
+        pass
+    return None
+
+
+def host_cpu():
+    """(model name, logical CPUs) of the host, from lscpu or /proc/cpuinfo."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith(("model name", "cpu part")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    import platform
+    return f"{model or 'unknown'} ({platform.machine()})", os.cpu_count() or 1
 
 
 # DRAM bytes (read + write) of one decode launch of this bench's default
@@ -180,9 +218,12 @@ def workload_config(wl, g, lanes_per_rank, ws, gc_interval):
     # and output label columns)
     lp_mb = lanes_per_rank * wl.T * wl.V * (2 if wl.dtype == "f16" else 4) / 1e6
     graph_mb = (20 * g["num_states"] + 28 * g["num_arcs"]) / 1e6
-    big = lp_mb + graph_mb > L2_MB
-    l2 = (f"inputs {'larger than' if big else 'within'} L2 ({L2_MB} MB): {lp_mb:.0f} MB log-probs per rank, "
-          f"{graph_mb:.0f} MB graph; no flush" + ("" if big else " (a small case, L2-resident)"))
+    l2b = l2_bytes()
+    l2_mb = l2b / 1e6 if l2b else None
+    big = l2_mb is not None and lp_mb + graph_mb > l2_mb
+    where = f"L2 ({l2_mb:.0f} MB, cudaDevAttrL2CacheSize)" if l2_mb else "L2 (size not queried: no device)"
+    l2 = (f"inputs {'larger than' if big else 'against'} {where}: {lp_mb:.0f} MB log-probs per rank, "
+          f"{graph_mb:.0f} MB graph; no flush" + ("" if big or l2_mb is None else " (a small case, L2-resident)"))
     return {"workload": workload_name(wl), "graph": f"{g['num_states']} states / {g['num_arcs']} arcs",
             "global_batch": lanes_per_rank * ws, "frames_per_utt": wl.T, "vocab": wl.V,
             "log_probs": wl.dtype, "search_beam": wl.search_beam, "max_active": wl.max_active,
@@ -221,13 +262,35 @@ def sample_text(s):
             f"one lane per thread")
 
 
+def single_thread(s, lanes=2):
+    """The oracle on one host thread: the first `lanes` lanes of the sample
+    decoded one after the other (frames/s, sample text)."""
+    import oracle
+    k = min(lanes, len(s["lanes"]))
+    t0 = time.perf_counter()
+    oracle.decode_batch(s["OG"], s["lp"][:k], s["lens"][:k], s["p"], threads=1)
+    dt = time.perf_counter() - t0
+    frames = int(sum(s["lens"][:k]))
+    return frames / dt, f"{k} lanes ({frames} frames) one after the other on 1 thread"
+
+
+def cpu_fields(s):
+    """Host description and the single-thread figure, for both arms."""
+    model, nproc = host_cpu()
+    v1, txt1 = single_thread(s)
+    return {"cpu_model": model, "nproc": nproc, "single_thread_value": v1, "single_thread_sample": txt1}
+
+
 def cpu_baseline(wi, threads=None):
     """The oracle as it stands, on the host cores, over a bounded sample of
-    lanes of the same workload (one lane per thread)."""
+    lanes of the same workload (one lane per thread), with its single-thread
+    figure beside it."""
     s = oracle_sample(wi, threads)
     dt, frames, arcs = oracle_run(s)
-    return {"value": frames / dt, "unit": "frames/s", "cores": len(s["lanes"]), "kind": "oracle",
-            "sample": sample_text(s), "arcs_per_s": arcs / dt, "seconds": dt}
+    out = {"value": frames / dt, "unit": "frames/s", "cores": len(s["lanes"]), "kind": "oracle",
+           "sample": sample_text(s), "arcs_per_s": arcs / dt, "seconds": dt}
+    out.update(cpu_fields(s))
+    return out
 
 
 def run_reference(args):
@@ -246,15 +309,16 @@ def run_reference(args):
             arcs_tot += arcs
     value = frames_tot / sum(times)
     cores = len(s["lanes"])
+    cpu_extra = cpu_fields(s)
     line = {
         "impl": "reference", "metric": "frames/s", "value": value, "unit": "frames/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": DTYPE, "dtype_note": DTYPE_NOTE, "data": "synthetic",
         "config": workload_config(wl, s["g"], args.lanes or wl.B, args.gpus, args.gc_interval),
         "arcs_expanded_per_s": arcs_tot / sum(times),
-        "cpu_baseline": {"value": value, "unit": "frames/s", "cores": cores, "kind": "oracle",
-                         "sample": sample_text(s) + f", {args.steps} timed passes"},
+        "cpu_baseline": dict({"value": value, "unit": "frames/s", "cores": cores, "kind": "oracle",
+                              "sample": sample_text(s) + f", {args.steps} timed passes"}, **cpu_extra),
         "e2e": {"value": value, "unit": "frames/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -381,12 +445,13 @@ def run_gpu(args):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.workload)
-        cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample", "cpu_model", "nproc",
+                                   "single_thread_value", "single_thread_sample")}
     line = {
         "metric": "frames/s", "value": value, "unit": "frames/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE,
+        "dtype_note": DTYPE_NOTE, "data": "synthetic",
         "config": workload_config(wl, g, B, ws, args.gc_interval),
         "arcs_expanded_per_s": arcs_per_s,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

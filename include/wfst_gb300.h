@@ -207,8 +207,11 @@ int wfst_decode(wfst_decoder* d, const void* log_probs, int32_t dtype, int64_t s
  * redirect) whose best complete path is within output_beam of the best path
  * (§3: output_beam acts only in this backward prune, never on the forward
  * search; §7).
- * Records are sorted by (t, src_state, arc_id).  *n_records receives the
- * true count; at most `cap` records are written.  Errors: INVALID_ARG, STATE.
+ * Records are sorted by (t, src_state, arc_id) and each such triple occurs
+ * once (an epsilon arc is one record per source token, evaluated with the
+ * token's final score, however many closure passes relaxed it).
+ * *n_records receives the true count; at most `cap` records are written.
+ * Errors: INVALID_ARG, STATE.
  */
 int wfst_lattice_export(wfst_decoder* d, int32_t lane, wfst_lat_record* out, int64_t cap,
                         int64_t* n_records);
@@ -300,25 +303,43 @@ int wfst_stats(wfst_decoder* d, int64_t* out, int32_t n);
 int wfst_mem_stats(wfst_decoder* d, int64_t* out, int32_t n);
 
 /*
+ * Test hook for the failure path of the device-side grid barrier (§5: the
+ * step loop's phases are separated by barriers; here every wait on one is
+ * bounded).  Arms the decoder's NEXT call only: each grid barrier of that
+ * launch waits for one arrival more than the grid makes, with a limit of
+ * timeout_ns instead of 4 s.  The first wait therefore gives up, sets the
+ * abort flag, and every CTA returns; the call returns WFST_ERR_TIMEOUT
+ * after wiping the decoder's per-state tables and closing its streaming
+ * channels, exactly as after a real timeout.  Later calls run normally.
+ * Nothing faults, traps or waits without a bound.
+ * Errors: INVALID_ARG (NULL decoder, timeout_ns outside [1 ms, 4 s]).
+ */
+int wfst_test_barrier_timeout(wfst_decoder* d, int64_t timeout_ns);
+
+/*
  * Offline decode that allocates nothing (no device or pinned memory, no
- * decoder object).  "GPU WFST Beam-Search Decoder" has no counterpart: its
- * decoder sizes a workspace per decoder (§6.1).  This is the same decode
- * as wfst_decode for callers that may not allocate once running (their own
- * memory pool, a real-time thread): its working memory is one region of
- * WFST_STATIC_SCRATCH_BYTES that the library declares statically, one per
- * device per process.
+ * decoder object).  The web page "GPU WFST Beam-Search Decoder" has no
+ * counterpart for it.  This is the same decode as wfst_decode for callers
+ * that may not allocate once running (their own memory pool, a real-time
+ * thread): its working memory is one region of WFST_STATIC_SCRATCH_BYTES
+ * that the library declares statically, one per device per process.
  * Arguments as in wfst_decode, with the decoder replaced by the graph and
  * its params: lattice and streaming must be 0; log_probs must be device
- * memory on the graph's device; B <= WFST_STATIC_MAX_LANES; frontier and
- * log capacities are never exceeded (frontier = num_states).
+ * memory on the graph's device; B <= WFST_STATIC_MAX_LANES.  The frontier
+ * holds every state; the winners log gets whatever the region has left
+ * after the call's other tables (at most one entry per state and frame) and
+ * cannot grow: a lane that fills it comes back with overflow bit 4 and the
+ * call returns CAPACITY, its outputs written and flagged (wfst_decode would
+ * grow the log and decode the lane again).
  * The first call on a device resolves the region's address and may load the
  * module there: make it before any stream capture begins.  The zero-start
  * part of the region (entries, marks, counters, barrier, results) is cleared
  * by every call.  Calls on one device are serialized by a lock held until
  * the results are on the host: calls that overlapped would race on the
  * region.
- * Errors: INVALID_ARG, CAPACITY (B or the call's tables exceed the region;
- * the message gives the bytes needed), CUDA, TIMEOUT.
+ * Errors: INVALID_ARG, CAPACITY (B or the call's tables exceed the region,
+ * the message giving the bytes needed; or a lane filled the winners log),
+ * CUDA, TIMEOUT.
  */
 #define WFST_STATIC_SCRATCH_BYTES (16u << 20)
 #define WFST_STATIC_MAX_LANES 8

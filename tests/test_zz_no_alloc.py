@@ -143,3 +143,35 @@ def test_static_rejects_what_does_not_fit(W):
     got = W.decode_static(G, params, lp[:1], lens)
     ref = W.Decoder(G, params, 1, wl.T).decode(lp[:1], lens)
     _same(got[0], ref[0], "after refusals")
+
+
+def test_static_log_fills_the_region_and_refuses_overflow(W):
+    """A wide beam on workload 1's graph (50k states): with max_active 10
+    the frontier decays after ~25 frames and a 60-frame lane needs about
+    1.08M winners-log entries, more than the decoder's default for that
+    max_active (1Mi) but within what the region leaves one lane, so the
+    static call equals wfst_decode and the oracle.  With max_active
+    unbounded every frame holds ~50k tokens (~3M entries): the static call
+    returns CAPACITY, while wfst_decode grows its log and stays exact."""
+    g = synth.make_graph(1)
+    G = W.Graph(g, device=0)
+    OG = oracle.Graph(g)
+    T = 60
+    lp = synth.make_log_probs(1, lanes=[0], T=T)
+    lens = np.array([T], np.int32)
+    for max_active, fits in ((10, True), (2**30, False)):
+        p = dict(search_beam=1000.0, output_beam=0.0, min_active=0, max_active=max_active,
+                 allow_partial=True, lattice=False)
+        params = _params(W, p)
+        D = W.Decoder(G, params, 1, T)
+        ref = D.decode(_cuda(lp), lens)
+        assert_lane_equal(ref[0], oracle_lane(OG, lp[0], T, p), f"decoder, max_active {max_active}")
+        for rep in range(2):
+            if fits:
+                got = W.decode_static(G, params, _cuda(lp), lens)
+                _same(got[0], ref[0], f"max_active {max_active} call {rep}")
+            else:
+                with pytest.raises(W.WfstError) as e:
+                    W.decode_static(G, params, _cuda(lp), lens)
+                assert e.value.code == -5 and "winners log" in str(e.value)
+        D.close()

@@ -36,7 +36,8 @@ LAT_DTYPE = np.dtype([("t", "<i4"), ("src_state", "<i4"), ("dst_state", "<i4"),
 EXPORTED = ["wfst_graph_upload", "wfst_graph_info", "wfst_graph_free", "wfst_decoder_create",
             "wfst_decoder_free", "wfst_decode", "wfst_lattice_export", "wfst_stream_create",
             "wfst_stream_advance", "wfst_stream_finalize", "wfst_stream_release", "wfst_stats",
-            "wfst_decode_static", "wfst_mem_stats", "wfst_blank_skip", "wfst_last_error"]
+            "wfst_decode_static", "wfst_mem_stats", "wfst_blank_skip", "wfst_test_barrier_timeout",
+            "wfst_last_error"]
 
 
 class WfstError(RuntimeError):
@@ -105,6 +106,7 @@ def load(build_if_missing: bool = False):
         L.wfst_stream_release.argtypes = [P, i32]
         L.wfst_stats.argtypes = [P, P, i32]
         L.wfst_mem_stats.argtypes = [P, P, i32]
+        L.wfst_test_barrier_timeout.argtypes = [P, i64]
         L.wfst_blank_skip.argtypes = [P, i32, i64, i64, i32, i32, C.c_float, P, i32, i32, P, P, P, P]
         for name in EXPORTED:
             if name not in ("wfst_last_error", "wfst_graph_free", "wfst_decoder_free"):
@@ -222,6 +224,10 @@ def wfst_stats(h):
     out = np.zeros(len(STAT_NAMES), np.int64)
     _check(load().wfst_stats(h, _ptr(out), len(STAT_NAMES)))
     return dict(zip(STAT_NAMES, out.tolist()))
+
+
+def wfst_test_barrier_timeout(h, timeout_ns):
+    _check(load().wfst_test_barrier_timeout(h, int(timeout_ns)))
 
 
 def wfst_mem_stats(h):
@@ -374,6 +380,11 @@ class Decoder:
 
     def stats(self):
         return wfst_stats(self.h)
+
+    def arm_barrier_timeout(self, timeout_ns=200_000_000):
+        """Test hook: the next call's grid barriers cannot complete and give
+        up after ``timeout_ns``; that call raises WfstError (TIMEOUT)."""
+        wfst_test_barrier_timeout(self.h, timeout_ns)
 
     def mem_stats(self):
         return wfst_mem_stats(self.h)

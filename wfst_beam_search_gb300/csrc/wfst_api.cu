@@ -288,6 +288,7 @@ struct wfst_decoder {
   std::vector<int32_t> chan_t;
   std::vector<int> lat_valid;
   int64_t stats[WFST_STAT_COUNT] = {0};
+  int64_t test_timeout_ns = 0;    // > 0: the next call's barriers cannot complete (test hook)
 };
 
 // Winners-log GC: the log of a lane is a ring whose size is a power of two
@@ -571,6 +572,9 @@ static int run_call(wfst_decoder* d, const void* lp, int32_t dtype, int64_t stri
   a.nblocks = d->grid[dtype == WFST_F16 ? 1 : 0];
   a.ub_skip = (d->p.options & WFST_OPT_NO_UB_SKIP) ? 0 : 1;
   a.gc_interval = d->p.gc_interval;
+  a.bar_extra = d->test_timeout_ns > 0 ? 1u : 0u;
+  a.timeout_ns = d->test_timeout_ns > 0 ? (unsigned long long)d->test_timeout_ns : kBarrierTimeoutNs;
+  d->test_timeout_ns = 0;  // one call only
   CU(cudaEventRecord(d->ev0, st), "event");
   CU(launch_decode(a, dtype, a.nblocks, st), "decode kernel launch");
   CU(cudaEventRecord(d->ev1, st), "event");
@@ -584,8 +588,11 @@ static int run_call(wfst_decoder* d, const void* lp, int32_t dtype, int64_t stri
      "words D2H");
   CU(cudaStreamSynchronize(st), "decode");
   if (d->h_bar->error & 1u) {
-    // the call was abandoned mid-way: every lane's state is void
+    // the call was abandoned mid-way: every lane's state is void (the entry
+    // tables and the epsilon dedupe marks, whose pass ids the lanes did not
+    // write back, start from zero again)
     cudaMemsetAsync(w.ent, 0, sizeof(ulonglong2) * 2 * L * (size_t)w.N, st);
+    if (w.mark) cudaMemsetAsync(w.mark, 0, sizeof(uint32_t) * L * (size_t)w.N, st);
     cudaStreamSynchronize(st);
     for (size_t l = 0; l < L; l++) {
       d->chan_state[l] = 0;
@@ -910,8 +917,17 @@ extern "C" int wfst_lattice_export(wfst_decoder* d, int32_t lane, wfst_lat_recor
     o[i].score = r.arcscore;
   }
   std::sort(o.begin(), o.end(), rec_less);
-  *n_records = (int64_t)n;
-  if (out && cap > 0) std::memcpy(out, o.data(), sizeof(wfst_lat_record) * std::min<int64_t>(cap, (int64_t)n));
+  // One record per (source token, arc): an epsilon arc of a token whose key
+  // changed during the closure without changing its score (a tie won by a
+  // lower arc id, or an improvement that landed before the token's own tile
+  // staged it) is relaxed in two passes with the same final score.  Both
+  // relaxations pass the device's final-score check and are identical.
+  size_t k = 0;
+  for (size_t i = 0; i < o.size(); i++)
+    if (k == 0 || rec_less(o[k - 1], o[i])) o[k++] = o[i];
+  o.resize(k);
+  *n_records = (int64_t)k;
+  if (out && cap > 0) std::memcpy(out, o.data(), sizeof(wfst_lat_record) * std::min<int64_t>(cap, (int64_t)k));
   return WFST_OK;
 }
 
@@ -1054,6 +1070,15 @@ extern "C" int wfst_stream_release(wfst_decoder* d, int32_t channel) {
   d->chan_state[channel] = 0;
   d->chan_t[channel] = 0;
   d->lat_valid[channel] = 0;
+  return WFST_OK;
+}
+
+extern "C" int wfst_test_barrier_timeout(wfst_decoder* d, int64_t timeout_ns) {
+  if (!d) return fail(WFST_ERR_INVALID_ARG, "test_barrier_timeout: NULL decoder");
+  if (timeout_ns < 1000000 || timeout_ns > (int64_t)kBarrierTimeoutNs)
+    return fail(WFST_ERR_INVALID_ARG, "test_barrier_timeout: timeout_ns must lie in [1 ms, 4 s]");
+  std::lock_guard<std::mutex> lock(d->mu);
+  d->test_timeout_ns = timeout_ns;
   return WFST_OK;
 }
 

@@ -16,6 +16,7 @@ constexpr int kOvfArena = 4;
 constexpr int kOvfKept = 16;
 constexpr int kOvfPath = 32;
 constexpr int kMaxGrowRounds = 12;  // offline capacity doublings per decode call
+constexpr unsigned long long kBarrierTimeoutNs = 4000000000ull;  // a grid barrier wait gives up after 4 s
 
 // lattice record flags
 constexpr int kRecEps = 1;
@@ -179,6 +180,8 @@ struct RunArgs {
   int32_t nblocks;
   int32_t ub_skip;                // upper-bound skips in the max/expand passes
   int32_t gc_interval;            // winners-log GC every gc_interval frames, 0 = off
+  uint32_t bar_extra;             // arrivals a grid barrier waits for beyond the grid (0; 1 = test hook)
+  unsigned long long timeout_ns;  // limit of one grid barrier wait
 };
 
 }  // namespace wfst

@@ -33,7 +33,6 @@
 
 namespace wfst {
 
-constexpr unsigned long long kTimeoutNs = 4000000000ull;  // 4 s per barrier wait
 constexpr int kSPT = kTile / 32;                           // slots per lane per tile
 constexpr int kCB = 5;                                     // tokens per thread per commit batch
 
@@ -267,13 +266,15 @@ __device__ __forceinline__ void prof_mark(unsigned long long* acc, int from, int
   }
 }
 
-// Bounded software grid barrier.  Returns false when the launch aborts.
+// Bounded software grid barrier.  Returns false when the launch aborts.  A
+// wait gives up after a.timeout_ns; a.bar_extra (0 except under the test
+// hook that exercises this path) raises the arrival target beyond the grid.
 __device__ bool grid_sync(const RunArgs& a, Smem& S, unsigned& epoch) {
   __syncthreads();
   if (threadIdx.x == 0) {
     GridBar* bar = a.w.bar;
     epoch++;
-    const unsigned target = epoch * (unsigned)gridDim.x;
+    const unsigned target = epoch * (unsigned)gridDim.x + a.bar_extra;
     __threadfence();
     atomicAdd(&bar->count, 1u);
     int ab = 0;
@@ -282,7 +283,7 @@ __device__ bool grid_sync(const RunArgs& a, Smem& S, unsigned& epoch) {
       const unsigned c = ld_acquire(&bar->count);
       if ((int)(c - target) >= 0) break;
       if (ld_acquire(&bar->abort)) { ab = 1; break; }
-      if (gtimer() - t0 > kTimeoutNs) {
+      if (gtimer() - t0 > a.timeout_ns) {
         atomicExch(&bar->abort, 1u);
         atomicOr(&bar->error, 1u);
         ab = 1;

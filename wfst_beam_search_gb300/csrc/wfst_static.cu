@@ -8,17 +8,21 @@
 // behind that pool's back, a real-time audio thread that must not block in
 // the allocator, or an embedding that sizes device memory once at start-up.
 // The web page "GPU WFST Beam-Search Decoder" has no counterpart for this
-// entry point: its decoder sizes a workspace per decoder (§6.1); this is the
-// same decode kernel fed from a fixed region.
+// entry point; it runs the same decode kernel as wfst_decode.
 //
 // The region is file-scope `__device__` storage of kScratchBytes.  Its
 // address is taken once per device (with that device current) through
 // cudaGetSymbolAddress; that first lookup may load the module onto the
 // device, so make the first call before any stream capture begins.
 //
-// Limits: B <= kStaticLanes lanes, lattice and streaming off, and every table
-// of the call (sized from B, T, the graph and words_cap) must fit the region;
-// a call that does not fit returns WFST_ERR_CAPACITY with the bytes it needed.
+// Limits: B <= kStaticLanes lanes, lattice and streaming off, and the call's
+// fixed tables (sized from B, T, the graph and words_cap) must fit the region;
+// a call that does not fit returns WFST_ERR_CAPACITY with the bytes it
+// needed.  The winners log gets the rest of the region, up to the most a
+// call can use (one entry per state and frame).  It cannot grow: a lane that
+// fills it comes back with overflow bit 4, and the call then returns
+// WFST_ERR_CAPACITY (the outputs are still written, flagged), where
+// wfst_decode would grow the log and decode the lane again.
 //
 // Zeroing: the recombination entries, the epsilon dedupe marks, the frame and
 // worklist counters, the grid barrier, the statistics and the result slots
@@ -28,9 +32,9 @@
 //
 // Concurrency: the region is one per device per process.  Two calls on the
 // same device that overlapped would race on it, so the call holds a
-// per-device lock from its first write of the region until its results are
-// on the host (it returns only after its stream work has finished).  Separate
-// processes each have their own region.
+// per-device lock from its first write of the region until its stream work
+// has finished — on every return path, errors included.  Separate processes
+// each have their own region.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -106,10 +110,10 @@ struct Carve {
   }
 };
 
-// Lays the call's tables out from `base` (nullptr: size only).  Returns the
-// total bytes and, in *zero_bytes, the length of the front part that must
-// start at zero.
-size_t layout(unsigned char* base, const DevGraph& G, int L, int T, const wfst_params& p, int words_cap,
+// Lays the call's tables out from `base` (nullptr: size only) with a winners
+// log of `log_cap` entries per lane.  Returns the total bytes and, in
+// *zero_bytes, the length of the front part that must start at zero.
+size_t layout(unsigned char* base, const DevGraph& G, int L, int T, int64_t log_cap, int words_cap,
               DevWork& w, LaneCall** calls, size_t* zero_bytes) {
   Carve c{base};
   const size_t N = (size_t)G.N;
@@ -118,11 +122,7 @@ size_t layout(unsigned char* base, const DevGraph& G, int L, int T, const wfst_p
   w.L = L;
   w.N = G.N;
   w.qcap = G.N;
-  // one frame holds at most qcap tokens, so mf * qcap entries never overflow;
-  // below that, the decoder's default log size
-  const int64_t log_bound = mf * w.qcap;
-  const int64_t log_default = std::max<int64_t>(mf * 4 * std::max(p.max_active, 1), 1 << 20);
-  w.log_cap = std::min(log_bound, log_default);
+  w.log_cap = log_cap;
   w.log_mask = ~0ull;  // a flat log (no winners-log GC here)
   w.lat_cap = 0;
   w.path_cap = 4 * mf * (1 + (int64_t)G.eps_depth);
@@ -151,10 +151,10 @@ size_t layout(unsigned char* base, const DevGraph& G, int L, int T, const wfst_p
     w.wl = c.take<TokRec>(2 * (size_t)L * w.qcap);
     w.wl_tile_first = c.take<int32_t>(2 * (size_t)L * w.tiles_cap);
   }
-  w.wlog = c.take<int2>((size_t)L * w.log_cap);
   w.path = c.take<int32_t>((size_t)L * w.path_cap);
   w.pframe = c.take<int2>((size_t)L * mf);
   w.words = c.take<int32_t>((size_t)L * words_cap);
+  w.wlog = c.take<int2>((size_t)L * w.log_cap);  // last: it takes what is left
   return (c.off + 255) & ~(size_t)255;
 }
 
@@ -194,6 +194,17 @@ struct DeviceGuard {
     cudaError_t e_ = (call);                             \
     if (e_ != cudaSuccess) return api_cuda_fail(e_, what); \
   } while (0)
+
+// Waits for the call's stream work on every return once armed, so that the
+// per-device lock (released after this guard) is never given up while a
+// kernel or a copy of this call still uses the region.
+struct StreamDrain {
+  cudaStream_t st;
+  bool armed = false;
+  ~StreamDrain() {
+    if (armed) cudaStreamSynchronize(st);
+  }
+};
 
 }  // namespace
 
@@ -244,21 +255,30 @@ extern "C" int wfst_decode_static(const wfst_graph* g, const wfst_params* params
   DevWork w;
   LaneCall* calls = nullptr;
   size_t zero_bytes = 0;
-  const size_t need = layout(nullptr, *G, B, T, *params, wc, w, &calls, &zero_bytes);
-  if (need > kScratchBytes) {
+  // the fixed tables with a log of one entry per frame, then the log takes
+  // the rest of the region up to one entry per state and frame
+  const int64_t mf = (int64_t)T + 2;
+  const size_t fixed = layout(nullptr, *G, B, T, mf, wc, w, &calls, &zero_bytes);
+  if (fixed > kScratchBytes) {
     char msg[160];
     snprintf(msg, sizeof(msg), "decode_static: the call needs %zu bytes of scratch, above WFST_STATIC_SCRATCH_BYTES (%zu)",
-             need, kScratchBytes);
+             fixed, kScratchBytes);
     return api_fail(WFST_ERR_CAPACITY, msg);
   }
+  const int64_t log_bound = mf * (int64_t)G->N;
+  const int64_t log_room = mf + (int64_t)((kScratchBytes - fixed) / (sizeof(int2) * (size_t)B));
+  const int64_t log_cap = std::min<int64_t>(std::min(log_bound, log_room), (int64_t)INT32_MAX - 1);
 
   DeviceSlot& slot = g_slots[device];
   std::lock_guard<std::mutex> lock(slot.mu);
   DeviceGuard dgd(device);
   int rc = setup_device(slot);
   if (rc != WFST_OK) return rc;
-  layout(slot.base, *G, B, T, *params, wc, w, &calls, &zero_bytes);
+  const size_t used = layout(slot.base, *G, B, T, log_cap, wc, w, &calls, &zero_bytes);
+  if (used > kScratchBytes) return api_fail(WFST_ERR_CAPACITY, "decode_static: internal layout error");
   cudaStream_t st = (cudaStream_t)stream;
+  StreamDrain drain{st};  // destroyed before `lock`: the stream is drained first
+  drain.armed = true;
   CUS(cudaMemsetAsync(slot.base, 0, zero_bytes, st), "decode_static: scratch clear");
   static_prepare<<<1, 32, 0, st>>>(w.lanes, calls, lv, B);
   CUS(cudaGetLastError(), "decode_static: lane set-up launch");
@@ -279,6 +299,7 @@ extern "C" int wfst_decode_static(const wfst_graph* g, const wfst_params* params
   a.lattice = 0;
   a.nblocks = slot.grid[dtype == WFST_F16 ? 1 : 0];
   a.ub_skip = (params->options & WFST_OPT_NO_UB_SKIP) ? 0 : 1;
+  a.timeout_ns = kBarrierTimeoutNs;
   CUS(launch_decode(a, dtype, a.nblocks, st), "decode_static: decode kernel launch");
   // results into host stack memory (pageable copies; the call then waits)
   Result res[kStaticLanes];
@@ -294,14 +315,18 @@ extern "C" int wfst_decode_static(const wfst_graph* g, const wfst_params* params
   if (bar.error & 2u) return api_fail(WFST_ERR_CUDA, "decode_static: epsilon closure did not converge");
   if (bar.error & 4u)
     return api_fail(WFST_ERR_TIMEOUT, "decode_static: a recombination CAS loop gave up after its retry bound");
+  // words of every lane; a copy error is reported only after the stream has
+  // drained, so no copy is left running when the call returns
+  cudaError_t copy_err = cudaSuccess;
+  int32_t short_lane = -1;
   for (int32_t b = 0; b < B; b++) {
     const Result& r = res[b];
     const int32_t nw = r.ok ? r.n_words : 0;
     if (words && words_cap > 0 && nw > 0) {
       const int32_t k = std::min(nw, words_cap);
-      CUS(cudaMemcpyAsync(words + (size_t)b * words_cap, w.words + (size_t)b * wc, sizeof(int32_t) * k,
-                          cudaMemcpyDeviceToHost, st),
-          "decode_static: words D2H");
+      const cudaError_t e = cudaMemcpyAsync(words + (size_t)b * words_cap, w.words + (size_t)b * wc,
+                                            sizeof(int32_t) * k, cudaMemcpyDeviceToHost, st);
+      if (e != cudaSuccess && copy_err == cudaSuccess) copy_err = e;
     }
     if (word_lens) word_lens[b] = nw;
     if (scores) scores[b] = r.ok ? (double)r.score : -INFINITY;
@@ -310,7 +335,19 @@ extern "C" int wfst_decode_static(const wfst_graph* g, const wfst_params* params
       meta[3 * b + 1] = r.reached_final;
       meta[3 * b + 2] = lanes[b].overflow;
     }
+    if (lanes[b].overflow && short_lane < 0) short_lane = b;
   }
-  CUS(cudaStreamSynchronize(st), "decode_static");
+  const cudaError_t sync_err = cudaStreamSynchronize(st);
+  drain.armed = false;
+  if (copy_err != cudaSuccess) return api_cuda_fail(copy_err, "decode_static: words D2H");
+  if (sync_err != cudaSuccess) return api_cuda_fail(sync_err, "decode_static");
+  if (short_lane >= 0) {
+    char msg[200];
+    snprintf(msg, sizeof(msg),
+             "decode_static: lane %d ran out of the region's winners log (%lld entries per lane; overflow bits %d); "
+             "wfst_decode grows it",
+             (int)short_lane, (long long)log_cap, (int)lanes[short_lane].overflow);
+    return api_fail(WFST_ERR_CAPACITY, msg);
+  }
   return WFST_OK;
 }
