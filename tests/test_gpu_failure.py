@@ -81,7 +81,7 @@ def test_streaming_barrier_timeout_closes_channels(W):
     p = wl_params(wl, lattice=False)
     T, chunk = 48, 16
     lp = synth.make_log_probs(0, lanes=range(2), T=T)
-    G, D = gpu_decoder(W, g, p, 2, chunk, streaming=True)
+    G, D = gpu_decoder(W, g, p, 2, T, streaming=True)   # path buffer for a whole-stream backtrack
     chans = [D.stream_create() for _ in range(2)]
     D.stream_advance(chans, _cuda(lp[:, :chunk]), np.full(2, chunk, np.int32), want_partial=True)
     D.arm_barrier_timeout(LIMIT_NS)
