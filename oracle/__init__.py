@@ -23,7 +23,7 @@ _HDR = os.path.join(_HERE, "wfst_oracle.h")
 
 REC_EPS, REC_FINAL, REC_REDIRECT = 1, 2, 4
 ST_NAMES = ["frames", "arcs_expanded", "sum_n", "sum_D", "sum_a", "sum_m", "max_n",
-            "max_D", "tokens", "records", "eps_relaxed", "finals"]
+            "max_D", "tokens", "records", "eps_relaxed", "finals", "records_dropped"]
 
 LAT_DTYPE = np.dtype([("t", "<i4"), ("src_state", "<i4"), ("dst_state", "<i4"),
                       ("arc_id", "<i4"), ("flags", "<i4"), ("score", "<f4")])
@@ -59,7 +59,8 @@ class _GraphDesc(C.Structure):
 class _Params(C.Structure):
     _fields_ = [("search_beam", C.c_float), ("output_beam", C.c_float),
                 ("min_active", C.c_int32), ("max_active", C.c_int32),
-                ("allow_partial", C.c_int32), ("lattice", C.c_int32)]
+                ("allow_partial", C.c_int32), ("lattice", C.c_int32),
+                ("lat_prune_interval", C.c_int32)]
 
 
 def lib():
@@ -136,10 +137,11 @@ class Graph:
 
 
 def params(search_beam=20.0, output_beam=8.0, min_active=30, max_active=10000,
-           allow_partial=True, lattice=False):
+           allow_partial=True, lattice=False, lat_prune_interval=0):
     return dict(search_beam=float(search_beam), output_beam=float(output_beam),
                 min_active=int(min_active), max_active=int(max_active),
-                allow_partial=bool(allow_partial), lattice=bool(lattice))
+                allow_partial=bool(allow_partial), lattice=bool(lattice),
+                lat_prune_interval=int(lat_prune_interval))
 
 
 class Decoder:
@@ -149,7 +151,7 @@ class Decoder:
         self.graph = graph
         self.p = p
         cp = _Params(p["search_beam"], p["output_beam"], p["min_active"], p["max_active"],
-                     int(p["allow_partial"]), int(p["lattice"]))
+                     int(p["allow_partial"]), int(p["lattice"]), int(p.get("lat_prune_interval", 0)))
         self._h = lib().or_dec_new(graph._h, C.byref(cp), -1 if t_eff is None else int(t_eff))
         if not self._h:
             raise MemoryError("oracle decoder allocation failed")

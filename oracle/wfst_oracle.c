@@ -45,6 +45,25 @@
  *     (arcscore + bwd[dst]) in reverse frame order (epsilon records of one
  *     frame in reverse epsilon-topological order); a record is kept iff
  *     end + bwd[dst] >= best - output_beam.
+ *   - interval lattice prune (§7 lat_prune_interval: every N frames a loose
+ *     prune over a window of recent frames, the final prune staying exact).
+ *     The page does not say which records it may drop; here it drops only
+ *     records the final prune can never keep.  After the step that makes
+ *     frame t (a positive multiple of N) the frontier, every frontier token
+ *     u gets beta(u) = -score(u); beta flows backward over the records of
+ *     the groups R_r = emit(r) + eps(r + 1), r in [max(-1, t - 2N), t - 1]
+ *     as bwd does (beta(src) = max over its records of arcscore +
+ *     beta(dst)).  A record of the window stays iff beta(dst) > -inf and
+ *     end + beta(dst) >= -((output_beam + 1) + 2^-12 |M|), M being the
+ *     exact max of the step that made frame t.  Every complete path passes
+ *     through one token u of frame t and its prefix score up to u is at most
+ *     score(u), so end + beta(dst) is minus the least amount by which a path
+ *     through the record falls behind the best path into its frontier
+ *     token; the final prune keeps a record only if some path through it is
+ *     within output_beam of the best complete path, which passes through
+ *     the frontier too, so only records with end + beta(dst) >= -output_beam
+ *     can be kept.  The margin 1 + 2^-12 |M| covers fp32 rounding of the
+ *     sums (|M| grows with the utterance).
  */
 #include "wfst_oracle.h"
 
@@ -245,10 +264,12 @@ typedef struct {
   int32_t arc;       /* arc id; A + s for final / redirect records */
   int32_t dst_tok;   /* -1: super-final node */
   int32_t dst_state; /* -1: super-final node */
-  int32_t flags;
+  int32_t flags;     /* OR_REC_*; REC_DROPPED: removed by an interval prune */
   float end;         /* forward value of the candidate */
   float arcscore;    /* the record's own score */
 } rec_t;
+
+#define REC_DROPPED 64
 
 struct or_dec {
   const or_graph* g;
@@ -257,6 +278,8 @@ struct or_dec {
   tok_t* tok;
   int64_t ntok, cap_tok;
   int64_t fb; /* first token of the current frame */
+  int64_t* fbase; /* first token of each frame 0..t */
+  int64_t cap_fbase;
   int32_t t;  /* frames consumed */
   float beam;
   int finalized;
@@ -285,6 +308,7 @@ void or_dec_free(or_dec* d) {
   free(d->rec);
   free(d->keep);
   free(d->trace);
+  free(d->fbase);
   free(d);
 }
 
@@ -384,6 +408,11 @@ or_dec* or_dec_new(const or_graph* g, const or_params* p, int32_t t_eff) {
     return NULL;
   }
   d->fb = 0;
+  if (grow((void**)&d->fbase, &d->cap_fbase, 1, sizeof(int64_t))) {
+    or_dec_free(d);
+    return NULL;
+  }
+  d->fbase[0] = 0;
   if (g->has_eps) {
     float cutoff0 = 0.0f - p->search_beam;
     if (closure(d, cutoff0) != OR_OK) {
@@ -393,6 +422,8 @@ or_dec* or_dec_new(const or_graph* g, const or_params* p, int32_t t_eff) {
   }
   return d;
 }
+
+static int interval_prune(or_dec* d, float M);
 
 /* One emitting step: consume the log-prob row `lp` (frame d->t). */
 static int step(or_dec* d, const float* lp) {
@@ -480,6 +511,8 @@ static int step(or_dec* d, const float* lp) {
   }
   d->fb = nb;
   d->t++;
+  if (grow((void**)&d->fbase, &d->cap_fbase, d->t + 1, sizeof(int64_t))) return OR_ENOMEM;
+  d->fbase[d->t] = nb;
   if (d->ncand > 0 && g->has_eps) {
     int rc = closure(d, cutoff);
     if (rc != OR_OK) return rc;
@@ -495,6 +528,11 @@ static int step(or_dec* d, const float* lp) {
   tr.next_size = (int32_t)m;
   if (grow((void**)&d->trace, &d->cap_trace, d->ntrace + 1, sizeof(or_step))) return OR_ENOMEM;
   d->trace[d->ntrace++] = tr;
+
+  if (d->p.lattice && d->p.lat_prune_interval > 0 && d->t % d->p.lat_prune_interval == 0) {
+    int rc = interval_prune(d, max_end);
+    if (rc != OR_OK) return rc;
+  }
 
   d->st[OR_ST_FRAMES]++;
   d->st[OR_ST_ARCS_EXPANDED] += d->ncand;
@@ -585,6 +623,64 @@ static int ord_cmp(const void* a, const void* b) {
   return x->r < y->r ? -1 : (x->r > y->r);
 }
 
+/* Interval lattice prune after the step that made frame d->t the frontier
+ * (§7 lat_prune_interval; the reading in this file's header): beta over the
+ * window's records backward from the frontier, in the final prune's order,
+ * then the window's records that no complete path within output_beam of
+ * the best can use are marked dropped.  M: the exact max of that step. */
+static int interval_prune(or_dec* d, float M) {
+  const or_graph* g = d->g;
+  const int32_t t = d->t, N = d->p.lat_prune_interval;
+  const int32_t r0 = t - 2 * N < -1 ? -1 : t - 2 * N;  /* oldest group of the window */
+  const int64_t tok0 = d->fbase[r0 < 0 ? 0 : r0];      /* first token of the window's nodes */
+  const int64_t nt = d->ntok - tok0;
+  float* beta = (float*)malloc(sizeof(float) * (size_t)(nt ? nt : 1));
+  ord_t* ord = (ord_t*)malloc(sizeof(ord_t) * (size_t)(d->nrec ? d->nrec : 1));
+  if (!beta || !ord) {
+    free(beta);
+    free(ord);
+    return OR_ENOMEM;
+  }
+  for (int64_t i = 0; i < nt; i++) beta[i] = -INFINITY;
+  for (int64_t i = d->fb; i < d->ntok; i++) beta[i - tok0] = -d->tok[i].score;
+  /* the window: emitting records of frames r0..t-1, epsilon records of
+   * frames r0+1..t (group R_r holds emit(r) and eps(r + 1)) */
+  int64_t nord = 0;
+  for (int64_t r = 0; r < d->nrec; r++) {
+    const rec_t* x = &d->rec[r];
+    if (x->flags & REC_DROPPED) continue;
+    const int eps = (x->flags & OR_REC_EPS) != 0;
+    const int32_t grp = eps ? x->frame - 1 : x->frame;
+    if (grp < r0 || grp > t - 1) continue;
+    ord[nord].r = r;
+    ord[nord].frame = x->frame;
+    ord[nord].cls = eps;
+    ord[nord].rank = eps ? g->eps_rank[d->tok[x->src_tok].state] : 0;
+    nord++;
+  }
+  qsort(ord, (size_t)nord, sizeof(ord_t), ord_cmp);
+  for (int64_t k = 0; k < nord; k++) {
+    const rec_t* x = &d->rec[ord[k].r];
+    const float v = x->arcscore + beta[x->dst_tok - tok0];
+    if (v > beta[x->src_tok - tok0]) beta[x->src_tok - tok0] = v;
+  }
+  const float margin = 0x1p-12f * fabsf(M);
+  const float room = d->p.output_beam + 1.0f;
+  const float lim = -(room + margin);
+  for (int64_t k = 0; k < nord; k++) {
+    rec_t* x = &d->rec[ord[k].r];
+    const float bd = beta[x->dst_tok - tok0];
+    const float tot = x->end + bd;
+    if (!(bd > -INFINITY && tot >= lim)) {
+      x->flags |= REC_DROPPED;
+      d->st[OR_ST_DROPPED]++;
+    }
+  }
+  free(beta);
+  free(ord);
+  return OR_OK;
+}
+
 /* backward output_beam prune over the persisted records (§3, §7) */
 static int prune_lattice(or_dec* d) {
   const or_graph* g = d->g;
@@ -597,14 +693,17 @@ static int prune_lattice(or_dec* d) {
     return OR_ENOMEM;
   }
   for (int64_t i = 0; i < d->ntok; i++) bwd[i] = -INFINITY;
+  int64_t nord = 0;
   for (int64_t r = 0; r < d->nrec; r++) {
-    ord[r].r = r;
-    ord[r].frame = d->rec[r].frame;
-    ord[r].cls = (d->rec[r].flags & OR_REC_EPS) ? 1 : 0;
-    ord[r].rank = (d->rec[r].flags & OR_REC_EPS) ? g->eps_rank[d->tok[d->rec[r].src_tok].state] : 0;
+    if (d->rec[r].flags & REC_DROPPED) continue;
+    ord[nord].r = r;
+    ord[nord].frame = d->rec[r].frame;
+    ord[nord].cls = (d->rec[r].flags & OR_REC_EPS) ? 1 : 0;
+    ord[nord].rank = (d->rec[r].flags & OR_REC_EPS) ? g->eps_rank[d->tok[d->rec[r].src_tok].state] : 0;
+    nord++;
   }
-  qsort(ord, (size_t)d->nrec, sizeof(ord_t), ord_cmp);
-  for (int64_t k = 0; k < d->nrec; k++) {
+  qsort(ord, (size_t)nord, sizeof(ord_t), ord_cmp);
+  for (int64_t k = 0; k < nord; k++) {
     const rec_t* r = &d->rec[ord[k].r];
     const float bd = r->dst_tok < 0 ? 0.0f : bwd[r->dst_tok];
     const float v = r->arcscore + bd;
@@ -613,6 +712,7 @@ static int prune_lattice(or_dec* d) {
   const float thr = d->best_score - d->p.output_beam;
   for (int64_t r = 0; r < d->nrec; r++) {
     const rec_t* x = &d->rec[r];
+    if (x->flags & REC_DROPPED) continue;
     const float bd = x->dst_tok < 0 ? 0.0f : bwd[x->dst_tok];
     const float tot = x->end + bd;
     d->keep[r] = (uint8_t)(tot >= thr);
@@ -687,12 +787,14 @@ static int64_t export_records(or_dec* d, or_lat_record* out, int64_t cap, int on
   if (!d->finalized || !d->p.lattice) return 0;
   int64_t n = 0;
   for (int64_t r = 0; r < d->nrec; r++) {
+    if (d->rec[r].flags & REC_DROPPED) continue;
     if (only_kept && !(d->ok && d->keep && d->keep[r])) continue;
     n++;
   }
   if (!out || cap < n) return n;
   int64_t k = 0;
   for (int64_t r = 0; r < d->nrec; r++) {
+    if (d->rec[r].flags & REC_DROPPED) continue;
     if (only_kept && !(d->ok && d->keep && d->keep[r])) continue;
     const rec_t* x = &d->rec[r];
     or_lat_record* o = &out[k++];

@@ -40,6 +40,7 @@ typedef struct {
   int32_t min_active, max_active;
   int32_t allow_partial;
   int32_t lattice;
+  int32_t lat_prune_interval; /* interval lattice prune every N frames, 0 = off */
 } or_params;
 
 typedef struct {
@@ -57,7 +58,7 @@ typedef struct {
 enum {
   OR_ST_FRAMES = 0, OR_ST_ARCS_EXPANDED, OR_ST_SUM_N, OR_ST_SUM_D, OR_ST_SUM_A,
   OR_ST_SUM_M, OR_ST_MAX_N, OR_ST_MAX_D, OR_ST_TOKENS, OR_ST_RECORDS,
-  OR_ST_EPS_RELAXED, OR_ST_FINALS, OR_ST_COUNT
+  OR_ST_EPS_RELAXED, OR_ST_FINALS, OR_ST_DROPPED, OR_ST_COUNT
 };
 
 typedef struct or_graph or_graph;

@@ -24,7 +24,8 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "wfst_oracle.c")
 HDR = os.path.join(ROOT, "oracle", "wfst_oracle.h")
-PINS = os.path.join(ROOT, "tests", "test_oracle_pins.py")
+PINS = [os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+        os.path.join(ROOT, "tests", "test_oracle_interval_prune.py")]
 
 # name -> [(text in the oracle, planted replacement), ...]; each text occurs once
 MUTANTS = {
@@ -111,6 +112,13 @@ MUTANTS = {
     "counters: admitted counts every candidate": [("d->st[OR_ST_SUM_A] += admitted;",
                                                    "d->st[OR_ST_SUM_A] += d->ncand;")],
     "counters: frontier after the step": [("d->st[OR_ST_SUM_N] += n;", "d->st[OR_ST_SUM_N] += m;")],
+    # §7: interval lattice prune (the conservative reading)
+    "interval: frontier tokens start at 0, not -score": [("beta[i - tok0] = -d->tok[i].score;",
+                                                           "beta[i - tok0] = 0.0f;")],
+    "interval: window of N frames": [("const int32_t r0 = t - 2 * N < -1 ? -1 : t - 2 * N;",
+                                      "const int32_t r0 = t - N < -1 ? -1 : t - N;")],
+    "interval: no safety margin": [("const float room = d->p.output_beam + 1.0f;",
+                                    "const float room = d->p.output_beam + 0.0f;")],
 }
 
 _CHILD = r"""
@@ -120,7 +128,8 @@ import oracle
 oracle._LIB_PATH = {lib!r}
 oracle.build = lambda force=False: {lib!r}
 import pytest
-sys.exit(pytest.main([{pins!r}, "-x", "-q", "-p", "no:cacheprovider", "-m", "not gpu"]))
+sys.exit(pytest.main([*{pins!r}, "-x", "-q", "-p", "no:cacheprovider", "-m", "not gpu",
+                      "-k", "not workloads_0_and_3"]))
 """
 
 
