@@ -95,7 +95,25 @@ typedef struct {
   int32_t streaming;      /* 1: decoder serves wfst_stream_* (online beam semantics) */
   int32_t options;        /* WFST_OPT_* bits, 0 = defaults */
   int32_t gc_interval;    /* winners-log GC every gc_interval frames per lane, 0 = off (§6.3, §8.1) */
+  int32_t lat_prune_interval; /* lattice = 1: interval lattice prune every N frames, 0 = off (§7) */
 } wfst_params;
+
+/*
+ * Interval lattice prune (params.lat_prune_interval = N > 0, lattice = 1;
+ * §7: every N frames a prune runs over a window of recent frames, the final
+ * output_beam prune staying exact).  When frame t (a positive multiple of
+ * N) is committed, the records of the groups R_r = emit(r) + eps(r + 1),
+ * r in [max(-1, t - 2N), t - 1], are tested against frame t's frontier:
+ * every frontier token u starts at beta(u) = -score(u), beta flows backward
+ * over the window (beta(src) = max of arcscore + beta(dst)), and a record
+ * stays iff beta(dst) > -inf and end + beta(dst) >= -((output_beam + 1) +
+ * 2^-12 |M|), M the exact max of the step that made frame t.  Every complete
+ * path passes one frontier token u with a prefix score of at most score(u),
+ * so only records the final prune can never keep are dropped (the margin
+ * covers fp32 rounding): the exported lattice is the same with or without
+ * it, and the arena holds far fewer records on long audio.  Dropped records
+ * are compacted out of the arena, group by group.
+ */
 
 /* Turn off the per-token upper-bound skips of the max and expand passes
  * (§5.3 "Upper-bound skip"; exact either way — for identity tests). */
@@ -280,7 +298,8 @@ int wfst_stream_release(wfst_decoder* d, int32_t channel);
  * max tiles, wait at the first barrier, expand tiles, final-step tasks, wait
  * at the second barrier */
 #define WFST_STAT_NS_PROLOGUE 15
-#define WFST_STAT_COUNT 23
+#define WFST_STAT_LAT_HELD 23     /* lattice records held in the arenas of the call's lanes at its end */
+#define WFST_STAT_COUNT 24
 int wfst_stats(wfst_decoder* d, int64_t* out, int32_t n);
 
 /*

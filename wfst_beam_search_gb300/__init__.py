@@ -26,7 +26,7 @@ REC_EPS, REC_FINAL, REC_REDIRECT = 1, 2, 4
 STAT_NAMES = ["frames", "arcs_expanded", "sum_n", "sum_D", "sum_a", "sum_m", "eps",
               "steps", "barriers", "kernel_ns", "ns_init", "ns_max", "ns_expand", "ns_closure",
               "ns_prune", "ns_prologue", "ns_commit", "ns_clear", "ns_max_tiles", "ns_wait_x",
-              "ns_expand_tiles", "ns_final", "ns_wait_y"]
+              "ns_expand_tiles", "ns_final", "ns_wait_y", "lattice_records_held"]
 ERRORS = {-1: "INVALID_ARG", -2: "CORRUPT_GRAPH", -3: "CUDA", -4: "OOM", -5: "CAPACITY",
           -6: "TIMEOUT", -7: "STATE"}
 
@@ -57,7 +57,7 @@ class Params(C.Structure):
     _fields_ = [("search_beam", C.c_float), ("output_beam", C.c_float),
                 ("min_active", C.c_int32), ("max_active", C.c_int32),
                 ("allow_partial", C.c_int32), ("lattice", C.c_int32), ("streaming", C.c_int32),
-                ("options", C.c_int32), ("gc_interval", C.c_int32)]
+                ("options", C.c_int32), ("gc_interval", C.c_int32), ("lat_prune_interval", C.c_int32)]
 
 
 class Capacity(C.Structure):
@@ -305,12 +305,13 @@ MEM_NAMES = ["bytes", "frontier_cap", "log_cap", "lattice_cap", "path_cap", "gro
 
 def make_params(search_beam=20.0, output_beam=8.0, min_active=30, max_active=10000,
                 allow_partial=True, lattice=False, streaming=False, options=0,
-                gc_interval=0) -> Params:
+                gc_interval=0, lat_prune_interval=0) -> Params:
     """gc_interval > 0 turns on the winners-log GC (a GC round every
-    gc_interval frames per lane; lattice must be off)."""
+    gc_interval frames per lane; lattice must be off); lat_prune_interval > 0
+    (lattice on) prunes the lattice arena every that many frames."""
     return Params(float(search_beam), float(output_beam), int(min_active), int(max_active),
                   int(bool(allow_partial)), int(bool(lattice)), int(bool(streaming)), int(options),
-                  int(gc_interval))
+                  int(gc_interval), int(lat_prune_interval))
 
 
 def _lp_args(lp):

@@ -363,6 +363,8 @@ extern "C" int wfst_decoder_create(wfst_graph* g, const wfst_params* params, int
       params->min_active < 0 || params->max_active < 0)
     return fail(WFST_ERR_INVALID_ARG, "decoder_create: beams must be positive and active bounds >= 0");
   if (params->gc_interval < 0) return fail(WFST_ERR_INVALID_ARG, "decoder_create: gc_interval must be >= 0");
+  if (params->lat_prune_interval < 0 || (params->lat_prune_interval > 0 && !params->lattice))
+    return fail(WFST_ERR_INVALID_ARG, "decoder_create: lat_prune_interval must be >= 0 and needs lattice = 1");
   if (params->gc_interval > 0 && params->lattice)
     return fail(WFST_ERR_INVALID_ARG,
                 "decoder_create: the winners-log GC needs lattice = 0 (lattice records refer to every frame's entries)");
@@ -434,6 +436,7 @@ extern "C" int wfst_decoder_create(wfst_graph* g, const wfst_params* params, int
     DA(w.lat, L * lat_cap, false);
     DA(w.lat_cnt, L, true);
     DA(w.lat_groups, L * (size_t)mf, true);
+    DA(w.lat_gtmp, L * (size_t)mf, false);
     DA(w.bwd, L * log_cap, false);
     DA(w.lat_out, L * lat_cap, false);
     DA(w.lat_out_n, L, true);
@@ -572,6 +575,7 @@ static int run_call(wfst_decoder* d, const void* lp, int32_t dtype, int64_t stri
   a.nblocks = d->grid[dtype == WFST_F16 ? 1 : 0];
   a.ub_skip = (d->p.options & WFST_OPT_NO_UB_SKIP) ? 0 : 1;
   a.gc_interval = d->p.gc_interval;
+  a.lat_interval = d->p.lattice ? d->p.lat_prune_interval : 0;
   a.bar_extra = d->test_timeout_ns > 0 ? 1u : 0u;
   a.timeout_ns = d->test_timeout_ns > 0 ? (unsigned long long)d->test_timeout_ns : kBarrierTimeoutNs;
   d->test_timeout_ns = 0;  // one call only
@@ -628,6 +632,7 @@ static int run_call(wfst_decoder* d, const void* lp, int32_t dtype, int64_t stri
     S[WFST_STAT_EPS] += (int64_t)x.eps;
     S[WFST_STAT_ARCS] += (int64_t)(x.sum_d + x.eps + x.finals);
     S[WFST_STAT_STEPS] = std::max<int64_t>(S[WFST_STAT_STEPS], (int64_t)x.steps);
+    S[WFST_STAT_LAT_HELD] += (int64_t)x.lat_held;
   }
   S[WFST_STAT_BARRIERS] = d->h_bar->epochs;
   S[WFST_STAT_KERNEL_NS] = (int64_t)(ms * 1e6);
@@ -748,6 +753,7 @@ static int grow_frames(wfst_decoder* d, int32_t T) {
   plan[np++] = {(void**)&w.maxlp, sizeof(float) * L * (size_t)std::max(nf, 1), nullptr, false};
   plan[np++] = {(void**)&w.pframe, sizeof(int2) * L * mf, nullptr, false};
   if (w.lattice) plan[np++] = {(void**)&w.lat_groups, sizeof(int64_t) * L * mf, nullptr, true};
+  if (w.lattice) plan[np++] = {(void**)&w.lat_gtmp, sizeof(int64_t) * L * mf, nullptr, false};
   if (path_cap != w.path_cap) plan[np++] = {(void**)&w.path, sizeof(int32_t) * L * (size_t)path_cap, nullptr, false};
   for (int i = 0; i < np; i++) {
     if (cudaMalloc(&plan[i].fresh, plan[i].bytes) != cudaSuccess ||
@@ -879,6 +885,15 @@ extern "C" int wfst_decode(wfst_decoder* d, const void* log_probs, int32_t dtype
     stats_add(acc, d->stats);
   }
   std::memcpy(d->stats, acc, sizeof(acc));
+  if (d->p.lattice) {  // records held after the last round (a re-run replaced a lane's records)
+    std::vector<unsigned long long> held(B);
+    CU(cudaMemcpyAsync(held.data(), d->w.lat_cnt, sizeof(unsigned long long) * B, cudaMemcpyDeviceToHost, st),
+       "lattice counts D2H");
+    CU(cudaStreamSynchronize(st), "lattice counts D2H");
+    d->stats[WFST_STAT_LAT_HELD] = 0;
+    for (int32_t b = 0; b < B; b++)
+      d->stats[WFST_STAT_LAT_HELD] += (int64_t)std::min<unsigned long long>(held[b], (unsigned long long)d->w.lat_cap);
+  }
   CU(cudaStreamSynchronize(st), "decode");
   return WFST_OK;
 }

@@ -87,6 +87,7 @@ struct LaneCall {                 // per lane, per call
 struct LaneStats {                // per lane, accumulated by the kernel (zeroed per call)
   unsigned long long frames, sum_n, sum_d, sum_a, sum_m, eps, finals;
   unsigned long long steps;
+  unsigned long long lat_held;    // lattice records in the lane's arena at the end of the call
 };
 
 struct LatRec {                   // 32 bytes
@@ -151,6 +152,7 @@ struct DevWork {
   LatRec* lat;                    // [L][lat_cap]
   unsigned long long* lat_cnt;    // [L] records appended
   int64_t* lat_groups;            // [L][max_frames+2] B_t: first record appended after frame t's closure
+  int64_t* lat_gtmp;              // [L][max_frames+2] interval prune: survivors, then write cursors, per group
   uint32_t* bwd;                  // [L][log_cap] ordered backward scores
   LatRec* lat_out;                // [L][lat_cap] kept records (compacted)
   unsigned long long* lat_out_n;  // [L]
@@ -180,6 +182,7 @@ struct RunArgs {
   int32_t nblocks;
   int32_t ub_skip;                // upper-bound skips in the max/expand passes
   int32_t gc_interval;            // winners-log GC every gc_interval frames, 0 = off
+  int32_t lat_interval;           // interval lattice prune every lat_interval frames, 0 = off
   uint32_t bar_extra;             // arrivals a grid barrier waits for beyond the grid (0; 1 = test hook)
   unsigned long long timeout_ns;  // limit of one grid barrier wait
 };

@@ -1123,37 +1123,33 @@ __device__ void row_maxima(const RunArgs& a, Smem& S) {
 
 // ------------------------------------------------------------------ lattice prune
 
-// Backward scores over the persisted records of every lane with s.closure
-// set, in reverse append order, then the keep test (§3: output_beam acts only
-// here) and compaction of the kept records.
-//   Append order per lane: R_{-1} = eps(0), then for t = 0..T-1
-//   R_t = emit(t) + eps(t+1), then R_T = final(T) (+ redirect).  B_t (the
-//   start of R_t) is recorded in lat_groups during frame t's commit phase.
-//   Backward group j: j = 0 -> R_T; j odd -> epsilon records of R_{T-1-(j-1)/2};
-//   j even (> 0) -> emitting records of R_{T-1-(j-2)/2}.
-__device__ bool lattice_prune(const RunArgs& a, Smem& S, unsigned& epoch) {
+// Backward max-plus sweep over persisted records, group by group, for every
+// lane with s.closure set.  Append order per lane: R_{-1} = eps(0), then for
+// t = 0..T-1 R_t = emit(t) + eps(t+1), then R_T = final(T) (+ redirect);
+// B_t (the start of R_t) is recorded in lat_groups during frame t's commit.
+//   final sweep: group 0 = R_T, then for k = 0, 1, ...: the epsilon records
+//     (k even) or the emitting records (k odd) of R_{T-1-k/2}, down to R_{-1};
+//   interval sweep: the same from R_{s.t-1} down to R_{s.res_hi}.
+// bwd[src] = max over the group's records of arcscore + bwd[dst] (dst -1:
+// the super-final node, 0).  Epsilon groups repeat until nothing changes.
+__device__ bool bwd_sweep(const RunArgs& a, Smem& S, unsigned& epoch, bool final_mode) {
   const DevWork& w = a.w;
   const DevGraph& g = a.g;
   const int L = a.nlanes;
   const int tid = threadIdx.x;
-  const int G = gridDim.x;
-  const int64_t gstride = (int64_t)G * kThreads;
+  const int64_t gstride = (int64_t)gridDim.x * kThreads;
   const int64_t gstart = (int64_t)blockIdx.x * kThreads + tid;
-  for (int l = 0; l < L; l++) {
-    const SmLane& s = S.lane[l];
-    if (!s.closure) continue;
-    const int64_t n = min(s.cursor, w.log_cap);
-    uint32_t* bw = w.bwd + (size_t)l * w.log_cap;
-    for (int64_t i = gstart; i < n; i += gstride) bw[i] = ord_f(-INFINITY);
-  }
   if (blockIdx.x == 0 && tid < 3) w.bar->changed[tid] = 0u;
   if (!grid_sync(a, S, epoch)) return false;
   int maxg = 0;
-  for (int l = 0; l < L; l++)
-    if (S.lane[l].closure) maxg = max(maxg, 2 * S.lane[l].t + 2);
+  for (int l = 0; l < L; l++) {
+    const SmLane& s = S.lane[l];
+    if (s.closure) maxg = max(maxg, final_mode ? 2 * s.t + 2 : 2 * (s.t - (int)s.res_hi));
+  }
   int pass_no = 0;
   for (int j = 0; j < maxg; j++) {
-    const bool eps_group = (j & 1) == 1;
+    const int kk = final_mode ? j - 1 : j;     // -1: the final group
+    const bool eps_group = kk >= 0 && (kk & 1) == 0;
     if (eps_group && !g.has_eps) continue;
     const int npass = eps_group ? g.eps_depth + 2 : 1;
     for (int pass = 0; pass < npass; pass++, pass_no++) {
@@ -1165,14 +1161,14 @@ __device__ bool lattice_prune(const RunArgs& a, Smem& S, unsigned& epoch) {
         const SmLane& s = S.lane[l];
         int64_t lo = 0, hi = 0;
         if (s.closure) {
-          const int T = s.t;
           const int64_t* B = w.lat_groups + (size_t)l * (w.max_frames + 2);
-          if (j == 0) {
-            lo = B[T];
+          if (kk < 0) {
+            lo = B[s.t];
             hi = (int64_t)min(__ldcg(&w.lat_cnt[l]), (unsigned long long)w.lat_cap);
           } else {
-            const int r = T - 1 - (j - 1) / 2;  // R_r, r >= -1
-            if (r >= -1) {
+            const int r = s.t - 1 - kk / 2;  // R_r
+            const int r_bot = final_mode ? -1 : (int)s.res_hi;
+            if (r >= r_bot) {
               lo = (r < 0) ? 0 : B[r];
               hi = B[r + 1];
             }
@@ -1190,7 +1186,7 @@ __device__ bool lattice_prune(const RunArgs& a, Smem& S, unsigned& epoch) {
         const LatRec rec = w.lat[(size_t)l * w.lat_cap + r];
         const int flags = rec.frame_flags & 15;
         if (flags & kRecDead) continue;
-        if (j > 0 && (((flags & kRecEps) != 0) != eps_group)) continue;
+        if (kk >= 0 && (((flags & kRecEps) != 0) != eps_group)) continue;
         uint32_t* bw = w.bwd + (size_t)l * w.log_cap;
         const float bd = rec.dst_tok < 0 ? 0.0f : unord_f(__ldcg(bw + rec.dst_tok));
         const unsigned ov = ord_f(__fadd_rn(rec.arcscore, bd));
@@ -1201,6 +1197,26 @@ __device__ bool lattice_prune(const RunArgs& a, Smem& S, unsigned& epoch) {
       if (eps_group && ld_acquire(&w.bar->changed[fl]) == 0u) break;
     }
   }
+  return true;
+}
+
+// Backward scores over the persisted records of every lane with s.closure
+// set (the final sweep), then the keep test (§3: output_beam acts only
+// here) and compaction of the kept records.
+__device__ bool lattice_prune(const RunArgs& a, Smem& S, unsigned& epoch) {
+  const DevWork& w = a.w;
+  const int L = a.nlanes;
+  const int tid = threadIdx.x;
+  const int64_t gstride = (int64_t)gridDim.x * kThreads;
+  const int64_t gstart = (int64_t)blockIdx.x * kThreads + tid;
+  for (int l = 0; l < L; l++) {
+    const SmLane& s = S.lane[l];
+    if (!s.closure) continue;
+    const int64_t n = min(s.cursor, w.log_cap);
+    uint32_t* bw = w.bwd + (size_t)l * w.log_cap;
+    for (int64_t i = gstart; i < n; i += gstride) bw[i] = ord_f(-INFINITY);
+  }
+  if (!bwd_sweep(a, S, epoch, true)) return false;
   // keep test and compaction
   const int lane = tid & 31;
   for (int l = 0; l < L; l++) {
@@ -1232,6 +1248,147 @@ __device__ bool lattice_prune(const RunArgs& a, Smem& S, unsigned& epoch) {
     }
   }
   return true;
+}
+
+// Interval lattice prune (§7 lat_prune_interval) of the lanes with s.closure
+// set, right after frame t = s.t was committed (its tokens are the winners-
+// log entries [s.cursor, s.cursor + s.n_cur) and their entries still hold
+// their final scores).  Only records the final prune can never keep are
+// dropped: every frontier token u of frame t starts at beta(u) = -score(u),
+// beta flows backward over the groups R_r, r in [max(-1, t - 2N), t - 1]
+// (the window), and a window record stays iff beta(dst) > -inf and
+// end + beta(dst) >= -((output_beam + 1) + 2^-12 |M|), M the exact max of
+// the step that made frame t.  A complete path through a record passes one
+// token u of frame t and its prefix up to u scores at most score(u), so
+// end + beta(dst) is minus the least amount by which a path through the
+// record falls behind the best path into its frontier token; the final
+// prune keeps only records within output_beam of the best complete path.
+// The margin covers fp32 rounding.  Survivors are compacted group by group
+// through the lane's lat_out region (unused until the final prune) and the
+// group bounds B_r rewritten.
+__device__ bool interval_prune(const RunArgs& a, Smem& S, unsigned& epoch) {
+  const DevWork& w = a.w;
+  const int L = a.nlanes;
+  const int tid = threadIdx.x;
+  const int64_t gstride = (int64_t)gridDim.x * kThreads;
+  const int64_t gstart = (int64_t)blockIdx.x * kThreads + tid;
+  const int N = a.lat_interval;
+  const size_t mf = (size_t)w.max_frames + 2;
+  for (int l = tid; l < L; l += kThreads) {
+    SmLane& s = S.lane[l];
+    if (!s.closure) continue;
+    s.res_hi = max(-1, s.t - 2 * N);                 // the window's oldest group
+    s.res_lo = w.lat_groups[(size_t)l * mf + s.t];  // the window's end before compaction
+  }
+  __syncthreads();
+  // (1) beta of every node a window record touches: -inf; group counters 0
+  for (int l = 0; l < L; l++) {
+    const SmLane& s = S.lane[l];
+    if (!s.closure) continue;
+    const int64_t* B = w.lat_groups + (size_t)l * mf;
+    const int64_t lo = s.res_hi < 0 ? 0 : B[s.res_hi], hi = B[s.t];
+    const LatRec* R = w.lat + (size_t)l * w.lat_cap;
+    uint32_t* bw = w.bwd + (size_t)l * w.log_cap;
+    for (int64_t r = lo + gstart; r < hi; r += gstride) {
+      const LatRec rec = R[r];
+      if (rec.frame_flags & kRecDead) continue;
+      bw[rec.src_tok] = ord_f(-INFINITY);
+      bw[rec.dst_tok] = ord_f(-INFINITY);
+    }
+    if (blockIdx.x == 0)
+      for (int k = tid; k <= s.t - (int)s.res_hi; k += kThreads) w.lat_gtmp[(size_t)l * mf + k] = 0;
+  }
+  if (!grid_sync(a, S, epoch)) return false;
+  // (2) the frontier: beta(u) = -score(u)
+  for (int l = 0; l < L; l++) {
+    const SmLane& s = S.lane[l];
+    if (!s.closure) continue;
+    const int par = s.t & 1;
+    uint32_t* bw = w.bwd + (size_t)l * w.log_cap;
+    for (int64_t p = gstart; p < s.n_cur; p += gstride) {
+      const int32_t st = __ldcg(&w.front[ql(w, par, l) + p].state);
+      const float sc = key_score(__ldcg(&ent_at(w, l, st, par)->x));
+      bw[s.cursor + p] = ord_f(-sc);
+    }
+  }
+  // (3) backward over the window's groups
+  if (!bwd_sweep(a, S, epoch, false)) return false;
+  // (4) the keep test; surviving records counted per group
+  for (int l = 0; l < L; l++) {
+    const SmLane& s = S.lane[l];
+    if (!s.closure) continue;
+    const unsigned mk = __ldcg(&fc_of(w, s.t - 1, l)->maxkey);
+    const float M = mk ? unord_f(mk) : -INFINITY;
+    const float lim = -__fadd_rn(__fadd_rn(a.output_beam, 1.0f), __fmul_rn(0x1p-12f, fabsf(M)));
+    const int64_t* B = w.lat_groups + (size_t)l * mf;
+    const int64_t lo = s.res_hi < 0 ? 0 : B[s.res_hi], hi = B[s.t];
+    LatRec* R = w.lat + (size_t)l * w.lat_cap;
+    const uint32_t* bw = w.bwd + (size_t)l * w.log_cap;
+    for (int64_t r = lo + gstart; r < hi; r += gstride) {
+      const LatRec rec = R[r];
+      bool keep = false;
+      if (!(rec.frame_flags & kRecDead)) {
+        const float bd = unord_f(__ldcg(bw + rec.dst_tok));
+        keep = bd > -INFINITY && __fadd_rn(rec.end, bd) >= lim;
+      }
+      if (keep) {
+        const int grp = (rec.frame_flags >> 4) - ((rec.frame_flags & kRecEps) ? 1 : 0);
+        atomicAdd(reinterpret_cast<unsigned long long*>(w.lat_gtmp) + (size_t)l * mf + (grp - (int)s.res_hi), 1ull);
+      } else {
+        R[r].frame_flags = rec.frame_flags | kRecDead;
+      }
+    }
+  }
+  if (!grid_sync(a, S, epoch)) return false;
+  // (5) new group starts (one thread per lane): B_r, and each group's
+  //     counter becomes its write cursor
+  if (blockIdx.x == 0)
+    for (int l = tid; l < L; l += kThreads) {
+      const SmLane& s = S.lane[l];
+      if (!s.closure) continue;
+      int64_t* B = w.lat_groups + (size_t)l * mf;
+      int64_t* cnt = w.lat_gtmp + (size_t)l * mf;
+      const int r0 = (int)s.res_hi;
+      int64_t pos = r0 < 0 ? 0 : B[r0];
+      for (int r = r0; r < s.t; r++) {
+        const int64_t c = cnt[r - r0];
+        cnt[r - r0] = pos;
+        if (r >= 0) B[r] = pos;
+        pos += c;
+      }
+      B[s.t] = pos;
+      w.lat_cnt[l] = (unsigned long long)pos;
+    }
+  if (!grid_sync(a, S, epoch)) return false;
+  // (6) survivors into the lane's lat_out region at their new positions
+  for (int l = 0; l < L; l++) {
+    const SmLane& s = S.lane[l];
+    if (!s.closure) continue;
+    const int64_t lo = s.res_hi < 0 ? 0 : w.lat_groups[(size_t)l * mf + s.res_hi];  // unchanged by (5)
+    const int64_t hi = s.res_lo;
+    const LatRec* R = w.lat + (size_t)l * w.lat_cap;
+    LatRec* O = w.lat_out + (size_t)l * w.lat_cap;
+    unsigned long long* cur = reinterpret_cast<unsigned long long*>(w.lat_gtmp) + (size_t)l * mf;
+    for (int64_t r = lo + gstart; r < hi; r += gstride) {
+      const LatRec rec = R[r];
+      if (rec.frame_flags & kRecDead) continue;
+      const int grp = (rec.frame_flags >> 4) - ((rec.frame_flags & kRecEps) ? 1 : 0);
+      const unsigned long long p = atomicAdd(cur + (grp - (int)s.res_hi), 1ull);
+      O[p - lo] = rec;
+    }
+  }
+  if (!grid_sync(a, S, epoch)) return false;
+  // (7) back into the arena
+  for (int l = 0; l < L; l++) {
+    const SmLane& s = S.lane[l];
+    if (!s.closure) continue;
+    const int64_t* B = w.lat_groups + (size_t)l * mf;
+    const int64_t lo = s.res_hi < 0 ? 0 : B[s.res_hi], hi = B[s.t];
+    LatRec* R = w.lat + (size_t)l * w.lat_cap;
+    const LatRec* O = w.lat_out + (size_t)l * w.lat_cap;
+    for (int64_t r = lo + gstart; r < hi; r += gstride) R[r] = O[r - lo];
+  }
+  return grid_sync(a, S, epoch);
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -1561,6 +1718,25 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     if (!grid_sync(a, S, epoch)) return;
     prof_mark(prof, tsub, kProfBarX);
     prof_mark(prof, tlast, kProfCommitMax);
+
+    // ================= interval lattice prune of the lanes whose frame t
+    // (committed above) is a positive multiple of the interval
+    if (lat && a.lat_interval > 0) {
+      int due = 0;
+      for (int l = tid; l < L; l += kThreads) {
+        SmLane& s = S.lane[l];
+        const int ovf = __ldcg(&w.lanes[l].overflow);
+        s.closure = (s.phase != kNone && s.need_commit && s.t > 0 && s.t % a.lat_interval == 0 &&
+                     !(ovf & (kOvfArena | kOvfKept)))
+                        ? 1 : 0;
+        due |= s.closure;
+      }
+      if (__syncthreads_or(due) && !interval_prune(a, S, epoch)) return;
+      for (int l = tid; l < L; l += kThreads) S.lane[l].closure = 0;
+      __syncthreads();
+      prof_mark(prof, tlast, kProfPrune);
+      if (blockIdx.x == 0 && tid == 0) prof[kProfSlots + tsub] = prof[kProfSlots + tlast];
+    }
 
     // ================= phase Y: expand (admit + recombine); final / partial
     if (tid == 0) S.tctr[0] = 0u;
@@ -1900,6 +2076,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
       ls.sum_d += s.sum_d;
       ls.sum_m += s.sum_m;
       ls.steps = steps;
+      if (lat) ls.lat_held = __ldcg(&w.lat_cnt[l]);
     }
     if (tid == 0) {
       w.bar->epochs = epoch;

@@ -213,8 +213,9 @@ extern "C" int wfst_decode_static(const wfst_graph* g, const wfst_params* params
                                   int32_t B, int32_t T, void* stream, int32_t* words, int32_t words_cap,
                                   int32_t* word_lens, double* scores, int32_t* meta) {
   if (!g || !params) return api_fail(WFST_ERR_INVALID_ARG, "decode_static: NULL graph or params");
-  if (params->lattice || params->streaming || params->gc_interval)
-    return api_fail(WFST_ERR_INVALID_ARG, "decode_static: lattice, streaming and gc_interval must be 0");
+  if (params->lattice || params->streaming || params->gc_interval || params->lat_prune_interval)
+    return api_fail(WFST_ERR_INVALID_ARG,
+                    "decode_static: lattice, streaming, gc_interval and lat_prune_interval must be 0");
   if (!(params->search_beam > 0.f) || std::isnan(params->output_beam) || params->output_beam < 0.f ||
       params->min_active < 0 || params->max_active < 0)
     return api_fail(WFST_ERR_INVALID_ARG, "decode_static: beams must be positive and active bounds >= 0");
