@@ -469,6 +469,8 @@ def run_gpu(args):
         "gpu_launches": args.steps * calls_per_step,
         "lanes_ok": res_ok,
         "lanes_overflowed": int((meta[:, 2] != 0).sum()),   # capacity bits left after growth (0 expected)
+        "decoder_memory": {k: v for k, v in W.wfst_mem_stats(D.h).items()
+                           if k in ("bytes", "reserved", "lazy_committed", "frontier_cap", "log_cap", "grows")},
         "clocks": clk,
         "cpu_baseline": cpu,
     }

@@ -123,8 +123,8 @@ typedef struct {
 
 /* Per-lane capacities; 0 in any field selects its default. */
 typedef struct {
-  int64_t frontier_cap;   /* tokens per lane per frame (default: num_states, never overflows) */
-  int64_t log_cap;        /* winners-log entries per lane (default (max_frames+2)*4*max_active, >= 1Mi) */
+  int64_t frontier_cap;   /* tokens per lane per frame (default min(num_states, max(64Ki, 16*max_active))) */
+  int64_t log_cap;        /* winners-log entries per lane (default (max_frames+2)*1.5*max_active, >= 1Mi) */
   int64_t lattice_cap;    /* lattice records per lane (default (max_frames+2)*2*max_active, >= 1Mi) */
   int64_t path_cap;       /* arcs of one best path (default 4*(max_frames+2)*(1 + epsilon depth);
                              with the GC, 4*max(max_frames+2, 1024)*(1 + epsilon depth)) */
@@ -178,9 +178,14 @@ void wfst_graph_free(wfst_graph* g);
  * Create a decoder with max_lanes lanes (utterances decoded together, or
  * streaming channels) for frames up to max_frames per lane (offline: per
  * call; streaming: per channel when lattice is on).  caps may be NULL.
- * All workspace is allocated here, once; decoding allocates nothing more
- * except a host-input staging buffer (see wfst_decode).
- * Errors: INVALID_ARG, CAPACITY (a table would exceed 2^31 entries), OOM, CUDA.
+ * The workspace is set up here: fixed tables are allocated; the frontier,
+ * winners-log and lattice tables reserve address space and commit device
+ * memory for their initial capacities (§6.2 lazily committed regions).
+ * Later calls commit more only when a capacity grows (an offline overflow,
+ * or a streaming channel past half of its winners log or lattice arena),
+ * plus a host-input staging buffer (see wfst_decode).
+ * Errors: INVALID_ARG, CAPACITY (a table would exceed 2^31 entries), OOM,
+ * CUDA (also when the device lacks virtual memory management).
  */
 int wfst_decoder_create(wfst_graph* g, const wfst_params* params, int32_t max_lanes,
                         int32_t max_frames, const wfst_capacity* caps, wfst_decoder** out);
@@ -307,8 +312,11 @@ int wfst_stats(wfst_decoder* d, int64_t* out, int32_t n);
  * WFST_MEM_COUNT): device bytes held, then the current per-lane capacities
  * (frontier tokens, winners-log entries, lattice records, best-path arcs) and
  * the number of capacity doublings so far, then max_frames (which offline
- * decodes of longer utterances raise).  §6.2 of the page reports the
- * decoder's memory the same way; here capacities only grow on demand.
+ * decodes of longer utterances raise), then the address space reserved for
+ * the lazily committed tables and the device memory committed to them.
+ * §6.2 of the page reports the decoder's memory the same way: the frontier,
+ * winners-log and lattice tables reserve worst-case address ranges and
+ * commit physical memory only for their current capacities.
  * Errors: INVALID_ARG (NULL pointers, n < 0).
  */
 #define WFST_MEM_BYTES 0
@@ -318,7 +326,9 @@ int wfst_stats(wfst_decoder* d, int64_t* out, int32_t n);
 #define WFST_MEM_PATH_CAP 4
 #define WFST_MEM_GROWS 5
 #define WFST_MEM_MAX_FRAMES 6    /* frames per call the per-frame tables hold now */
-#define WFST_MEM_COUNT 7
+#define WFST_MEM_RESERVED 7      /* address space reserved for the lazily committed tables */
+#define WFST_MEM_LAZY_COMMITTED 8 /* device memory committed to them (part of WFST_MEM_BYTES) */
+#define WFST_MEM_COUNT 9
 int wfst_mem_stats(wfst_decoder* d, int64_t* out, int32_t n);
 
 /*

@@ -300,7 +300,8 @@ class Graph:
 
 OPT_NO_UB_SKIP = 1
 OPT_NO_GROW = 4
-MEM_NAMES = ["bytes", "frontier_cap", "log_cap", "lattice_cap", "path_cap", "grows", "max_frames"]
+MEM_NAMES = ["bytes", "frontier_cap", "log_cap", "lattice_cap", "path_cap", "grows", "max_frames",
+             "reserved", "lazy_committed"]
 
 
 def make_params(search_beam=20.0, output_beam=8.0, min_active=30, max_active=10000,

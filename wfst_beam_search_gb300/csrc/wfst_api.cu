@@ -17,6 +17,7 @@
 
 #include "../../include/wfst_gb300.h"
 #include "wfst_internal.h"
+#include "wfst_vmm.h"
 
 namespace wfst {
 cudaError_t launch_decode(const RunArgs& a, int dtype, int grid, cudaStream_t st);
@@ -289,7 +290,71 @@ struct wfst_decoder {
   std::vector<int> lat_valid;
   int64_t stats[WFST_STAT_COUNT] = {0};
   int64_t test_timeout_ns = 0;    // > 0: the next call's barriers cannot complete (test hook)
+  // lazily committed tables (§6.2): worst-case address ranges, physical
+  // memory for the current capacities only; growth maps more after it
+  LazyRegions lz_front, lz_score, lz_wl;   // [2][L] regions, one stride (entries)
+  LazyRegions lz_log, lz_bwd;              // [L] regions, one stride
+  LazyRegions lz_lat, lz_lat_out;          // [L] regions, one stride
 };
+
+// Point the kernel's view at the lazy tables (their bases move when a
+// stride grows) and record their strides.
+static void sync_lazy(wfst_decoder* d) {
+  DevWork& w = d->w;
+  w.front = static_cast<TokRec*>(d->lz_front.base());
+  w.score = static_cast<float*>(d->lz_score.base());
+  w.wl = d->lz_wl.active() ? static_cast<TokRec*>(d->lz_wl.base()) : nullptr;
+  w.q_stride = d->lz_front.stride_entries();
+  w.wlog = static_cast<int2*>(d->lz_log.base());
+  w.bwd = d->lz_bwd.active() ? static_cast<uint32_t*>(d->lz_bwd.base()) : nullptr;
+  w.log_stride = d->lz_log.stride_entries();
+  w.lat = d->lz_lat.active() ? static_cast<LatRec*>(d->lz_lat.base()) : nullptr;
+  w.lat_out = d->lz_lat_out.active() ? static_cast<LatRec*>(d->lz_lat_out.base()) : nullptr;
+  w.lat_stride = d->lz_lat.active() ? d->lz_lat.stride_entries() : 0;
+}
+
+static int64_t lazy_committed(const wfst_decoder* d) {
+  const LazyRegions* r[] = {&d->lz_front, &d->lz_score, &d->lz_wl, &d->lz_log, &d->lz_bwd, &d->lz_lat, &d->lz_lat_out};
+  int64_t b = 0;
+  for (const LazyRegions* x : r)
+    if (x->active()) b += (int64_t)x->committed_bytes();
+  return b;
+}
+
+static int64_t lazy_reserved(const wfst_decoder* d) {
+  const LazyRegions* r[] = {&d->lz_front, &d->lz_score, &d->lz_wl, &d->lz_log, &d->lz_bwd, &d->lz_lat, &d->lz_lat_out};
+  int64_t b = 0;
+  for (const LazyRegions* x : r)
+    if (x->active()) b += (int64_t)x->reserved_bytes();
+  return b;
+}
+
+// Commit `entries` per region in every active table of a group that shares
+// one stride; when that passes the stride, first reserve a common larger
+// stride in each of them.  CAPACITY on failure (nothing the call had
+// committed is lost).
+static int lazy_commit(LazyRegions* const* group, int n, int64_t entries, int64_t floor_stride) {
+  std::string msg;
+  int64_t stride = 0;
+  for (int i = 0; i < n; i++)
+    if (group[i]->active()) stride = std::max(stride, group[i]->stride_entries());
+  if (entries > stride || floor_stride > stride) {
+    const int64_t want = std::max({entries, 2 * stride, floor_stride});
+    for (int i = 0; i < n; i++)
+      if (group[i]->active() && group[i]->reserve(want, &msg))
+        return fail(WFST_ERR_CAPACITY, "lazy tables: " + msg);
+    // tables of a group share one stride in entries
+    int64_t s = 0;
+    for (int i = 0; i < n; i++)
+      if (group[i]->active()) s = std::max(s, group[i]->stride_entries());
+    for (int i = 0; i < n; i++)
+      if (group[i]->active() && group[i]->stride_entries() != s && group[i]->reserve(s, &msg))
+        return fail(WFST_ERR_CAPACITY, "lazy tables: " + msg);
+  }
+  for (int i = 0; i < n; i++)
+    if (group[i]->active() && group[i]->commit(entries, &msg)) return fail(WFST_ERR_CAPACITY, "lazy tables: " + msg);
+  return WFST_OK;
+}
 
 // Winners-log GC: the log of a lane is a ring whose size is a power of two
 // (index & (size - 1)) of at most 2^29 entries, so that a signed chain step
@@ -335,6 +400,14 @@ static void decoder_destroy(wfst_decoder* d) {
   if (!d) return;
   {
     DeviceGuard dgd(d->g ? d->g->device : 0);
+    cudaDeviceSynchronize();
+    d->lz_front.release();
+    d->lz_score.release();
+    d->lz_wl.release();
+    d->lz_log.release();
+    d->lz_bwd.release();
+    d->lz_lat.release();
+    d->lz_lat_out.release();
     for (void* p : d->allocs) cudaFree(p);
     if (d->h_calls) cudaFreeHost(d->h_calls);
     if (d->h_res) cudaFreeHost(d->h_res);
@@ -371,10 +444,14 @@ extern "C" int wfst_decoder_create(wfst_graph* g, const wfst_params* params, int
   const bool gc = params->gc_interval > 0;
   const DevGraph& G = g->dg;
   const int64_t N = G.N;
-  int64_t qcap = (caps && caps->frontier_cap > 0) ? std::min<int64_t>(caps->frontier_cap, N) : N;
+  // lazily committed defaults: the frontier holds up to 16 * max_active
+  // tokens (at least 64Ki, at most N) and the winners log 1.5 * max_active
+  // entries per frame (at least 1Mi); both grow on overflow
+  const int64_t ma = std::max(params->max_active, 1);
+  int64_t qcap = (caps && caps->frontier_cap > 0) ? std::min<int64_t>(caps->frontier_cap, N)
+                                                  : std::min<int64_t>(N, std::max<int64_t>(65536, 16 * ma));
   const int64_t mf = (int64_t)max_frames + 2;
-  int64_t log_cap = (caps && caps->log_cap > 0) ? caps->log_cap
-                                                : std::max<int64_t>(mf * 4 * std::max(params->max_active, 1), 1 << 20);
+  int64_t log_cap = (caps && caps->log_cap > 0) ? caps->log_cap : std::max<int64_t>(mf * ma * 3 / 2, 1 << 20);
   log_cap = std::min<int64_t>(log_cap, (int64_t)INT32_MAX - 1);
   if (gc) log_cap = gc_ring_size(log_cap);
   const int64_t fin_cap = gc ? ((caps && caps->fin_cap > 0) ? std::min<int64_t>(caps->fin_cap, kMaxFinCap) : 65536) : 0;
@@ -413,32 +490,60 @@ extern "C" int wfst_decoder_create(wfst_graph* g, const wfst_params* params, int
   w.max_frames = max_frames;
   const size_t L = (size_t)max_lanes;
   cudaError_t e = cudaSuccess;
+  // the lazy tables: address space for the frontier's worst case (N tokens)
+  // and for 8x the initial log and lattice sizes; physical memory for the
+  // initial capacities
+  const size_t gran = LazyRegions::granularity(g->device);
+  if (!gran) {
+    decoder_destroy(d);
+    return fail(WFST_ERR_CUDA, "decoder_create: CUDA virtual memory management is not available on this device");
+  }
+  {
+    const int64_t q_align = (int64_t)(gran / sizeof(float));       // front, score and worklists share one stride
+    const int64_t log_align = (int64_t)(gran / sizeof(uint32_t));  // winners log and bwd share one stride
+    const int64_t lat_align = (int64_t)(gran / sizeof(LatRec));
+    d->lz_front.init(g->device, 2 * max_lanes, sizeof(TokRec), q_align);
+    d->lz_score.init(g->device, 2 * max_lanes, sizeof(float), q_align);
+    if (G.has_eps) d->lz_wl.init(g->device, 2 * max_lanes, sizeof(TokRec), q_align);
+    d->lz_log.init(g->device, max_lanes, sizeof(int2), log_align);
+    if (params->lattice) {
+      d->lz_bwd.init(g->device, max_lanes, sizeof(uint32_t), log_align);
+      d->lz_lat.init(g->device, max_lanes, sizeof(LatRec), lat_align);
+      d->lz_lat_out.init(g->device, max_lanes, sizeof(LatRec), lat_align);
+    }
+    LazyRegions* qg[] = {&d->lz_front, &d->lz_score, &d->lz_wl};
+    LazyRegions* lg[] = {&d->lz_log, &d->lz_bwd};
+    LazyRegions* ag[] = {&d->lz_lat, &d->lz_lat_out};
+    const int64_t log_bound = gc ? kMaxGcRing : (int64_t)INT32_MAX - 1;
+    int rc = lazy_commit(qg, 3, qcap, N);
+    if (rc == WFST_OK) rc = lazy_commit(lg, 2, log_cap, std::min<int64_t>(8 * log_cap, log_bound));
+    if (rc == WFST_OK && params->lattice) rc = lazy_commit(ag, 2, lat_cap, 8 * lat_cap);
+    if (rc != WFST_OK) {
+      const std::string msg = g_err;
+      decoder_destroy(d);
+      return fail(WFST_ERR_OOM, "decoder_create: " + msg);
+    }
+    sync_lazy(d);
+  }
 #define DA(ptr, n, z) \
   if (e == cudaSuccess) e = dalloc(d, &(ptr), (size_t)(n), z)
   DA(w.ent, 2 * L * N, true);
-  DA(w.tpos, L * N, false);
-  DA(w.front, 2 * L * qcap, false);
-  DA(w.score, 2 * L * qcap, false);
+  if (G.has_eps || params->lattice) DA(w.tpos, L * N, false);  // token positions: epsilon graphs, lattices
   DA(w.maxlp, L * (size_t)std::max(max_frames, 1), false);
   DA(w.tile_first, 2 * L * w.tiles_cap, false);
   if (G.has_eps) {
-    DA(w.wl, 2 * L * qcap, false);
     DA(w.wl_tile_first, 2 * L * w.tiles_cap, false);
     DA(w.mark, L * N, true);
   }
   DA(w.wl_cnt, 3 * L, true);
-  DA(w.wlog, L * log_cap, false);
   if (gc) DA(w.fin, L * fin_cap, false);
   DA(w.fcnt, 4 * L, true);
   DA(w.lanes, L, true);
   DA(w.stats, L, true);
   if (params->lattice) {
-    DA(w.lat, L * lat_cap, false);
     DA(w.lat_cnt, L, true);
     DA(w.lat_groups, L * (size_t)mf, true);
     DA(w.lat_gtmp, L * (size_t)mf, false);
-    DA(w.bwd, L * log_cap, false);
-    DA(w.lat_out, L * lat_cap, false);
     DA(w.lat_out_n, L, true);
   }
   DA(w.path, L * path_cap, false);
@@ -674,37 +779,49 @@ static void write_lane(wfst_decoder* d, int32_t lane, int32_t out_index, int32_t
 
 // Offline capacity growth: double the capacity behind each overflow seen
 // (winners log, lattice arena, frontier up to num_states, best path up to the
-// longest path a decode can have).  Every new array is allocated before any
-// old one is released, so a failed allocation leaves the decoder as it was.
-// WFST_ERR_CAPACITY when nothing can grow (sizes at their bounds, or device
-// memory exhausted): the lanes keep their overflow bits.
+// longest path a decode can have).  The winners log, lattice arena and
+// frontier tables are lazily committed regions: growing them maps more
+// physical memory after what each lane holds, so nothing is copied and no
+// lane's contents move (only the lanes that overflowed need to run again).
+// The best-path and finalized-word buffers are reallocated, every new array
+// before any old one is released.  WFST_ERR_CAPACITY when nothing can grow
+// (sizes at their bounds, or device memory exhausted): the lanes keep their
+// overflow bits.
 static int grow_capacities(wfst_decoder* d, bool g_log, bool g_lat, bool g_q, bool g_path) {
   DevWork& w = d->w;
   const size_t L = (size_t)d->L;
   const DevGraph& G = d->g->dg;
   struct Plan { void** slot; size_t bytes; void* fresh; };
-  Plan plan[10];
+  Plan plan[4];
   int np = 0;
-  int64_t log_cap = w.log_cap, lat_cap = w.lat_cap, qcap = w.qcap, path_cap = w.path_cap, fin_cap = w.fin_cap;
+  bool grew = false;
+  int64_t path_cap = w.path_cap, fin_cap = w.fin_cap;
   const int64_t path_bound = 2 * ((int64_t)d->max_frames + 2) * (1 + (int64_t)G.eps_depth);
   const bool gc = d->p.gc_interval > 0;
   const int64_t log_bound = gc ? kMaxGcRing : (int64_t)INT32_MAX - 1;
   if (g_log && w.log_cap < log_bound) {
-    log_cap = std::min<int64_t>(2 * w.log_cap, log_bound);
-    plan[np++] = {(void**)&w.wlog, sizeof(int2) * L * (size_t)log_cap, nullptr};
-    if (w.lattice) plan[np++] = {(void**)&w.bwd, sizeof(uint32_t) * L * (size_t)log_cap, nullptr};
+    const int64_t cap = std::min<int64_t>(2 * w.log_cap, log_bound);
+    LazyRegions* lg[] = {&d->lz_log, &d->lz_bwd};
+    if (lazy_commit(lg, 2, cap, 0) != WFST_OK) return WFST_ERR_CAPACITY;
+    w.log_cap = cap;
+    if (gc) w.log_mask = (unsigned long long)(cap - 1);
+    grew = true;
   }
   if (g_lat && w.lattice && w.lat_cap < ((int64_t)1 << 40)) {
-    lat_cap = 2 * w.lat_cap;
-    plan[np++] = {(void**)&w.lat, sizeof(LatRec) * L * (size_t)lat_cap, nullptr};
-    plan[np++] = {(void**)&w.lat_out, sizeof(LatRec) * L * (size_t)lat_cap, nullptr};
+    const int64_t cap = 2 * w.lat_cap;
+    LazyRegions* ag[] = {&d->lz_lat, &d->lz_lat_out};
+    if (lazy_commit(ag, 2, cap, 0) != WFST_OK) return WFST_ERR_CAPACITY;
+    w.lat_cap = cap;
+    grew = true;
   }
   if (g_q && w.qcap < (int64_t)G.N) {
-    qcap = std::min<int64_t>(2 * w.qcap, (int64_t)G.N);
-    plan[np++] = {(void**)&w.front, sizeof(TokRec) * 2 * L * (size_t)qcap, nullptr};
-    plan[np++] = {(void**)&w.score, sizeof(float) * 2 * L * (size_t)qcap, nullptr};
-    if (G.has_eps) plan[np++] = {(void**)&w.wl, sizeof(TokRec) * 2 * L * (size_t)qcap, nullptr};
+    const int64_t cap = std::min<int64_t>(2 * w.qcap, (int64_t)G.N);
+    LazyRegions* qg[] = {&d->lz_front, &d->lz_score, &d->lz_wl};
+    if (lazy_commit(qg, 3, cap, 0) != WFST_OK) return WFST_ERR_CAPACITY;
+    w.qcap = cap;
+    grew = true;
   }
+  sync_lazy(d);
   if (g_path && w.path_cap < path_bound) {
     path_cap = std::min<int64_t>(2 * w.path_cap, path_bound);
     plan[np++] = {(void**)&w.path, sizeof(int32_t) * L * (size_t)path_cap, nullptr};
@@ -713,7 +830,7 @@ static int grow_capacities(wfst_decoder* d, bool g_log, bool g_lat, bool g_q, bo
     fin_cap = std::min<int64_t>(2 * w.fin_cap, kMaxFinCap);
     plan[np++] = {(void**)&w.fin, sizeof(int32_t) * L * (size_t)fin_cap, nullptr};
   }
-  if (np == 0) return fail(WFST_ERR_CAPACITY, "decode: capacities are at their bounds");
+  if (np == 0 && !grew) return fail(WFST_ERR_CAPACITY, "decode: capacities are at their bounds");
   for (int i = 0; i < np; i++) {
     if (cudaMalloc(&plan[i].fresh, plan[i].bytes) != cudaSuccess) {
       cudaGetLastError();
@@ -722,11 +839,7 @@ static int grow_capacities(wfst_decoder* d, bool g_log, bool g_lat, bool g_q, bo
     }
   }
   for (int i = 0; i < np; i++) dswap(d, plan[i].slot, plan[i].fresh, plan[i].bytes);
-  w.log_cap = log_cap;
-  if (gc) w.log_mask = (unsigned long long)(log_cap - 1);
   w.fin_cap = fin_cap;
-  w.lat_cap = lat_cap;
-  w.qcap = qcap;
   w.path_cap = path_cap;
   d->grows++;
   return WFST_OK;
@@ -865,13 +978,9 @@ extern "C" int wfst_decode(wfst_decoder* d, const void* log_probs, int32_t dtype
     rc = grow_capacities(d, g_log, g_lat, g_q, g_path);
     if (rc == WFST_ERR_CAPACITY) break;  // already at the largest sizes: the bits stay set
     if (rc != WFST_OK) return rc;
-    // a regrown lattice arena has lost every lane's records: all lanes run again
-    if (g_lat && d->p.lattice) {
-      ran.resize(B);
-      for (int32_t b = 0; b < B; b++) ran[b] = b;
-    } else {
-      ran = over;
-    }
+    // the grown tables kept every lane's contents in place: only the lanes
+    // that overflowed run again
+    ran = over;
     for (int32_t l = 0; l < d->L; l++) d->h_calls[l].row = -1;
     for (int32_t b : ran) {
       LaneCall& c = d->h_calls[b];
@@ -898,6 +1007,33 @@ extern "C" int wfst_decode(wfst_decoder* d, const void* log_probs, int32_t dtype
   return WFST_OK;
 }
 
+// Streaming headroom: a channel cannot grow a table in the middle of a call,
+// but between calls the lazily committed winners log and lattice arena grow
+// in place (their contents stay where they are), so when an open channel
+// has used more than half of either, double it: a stream then overflows
+// only if one chunk adds more than half a table.  Not for the winners-log
+// GC's rings, whose index mask depends on their size.
+static int stream_headroom(wfst_decoder* d, cudaStream_t st) {
+  DevWork& w = d->w;
+  int64_t log_use = 0, lat_use = 0;
+  for (int32_t l = 0; l < d->L; l++)
+    if (d->chan_state[l] == 1) log_use = std::max<int64_t>(log_use, d->h_lanes[l].cursor - d->h_lanes[l].floor);
+  if (d->p.lattice) {
+    std::vector<unsigned long long> n(d->L);
+    CU(cudaMemcpyAsync(n.data(), w.lat_cnt, sizeof(unsigned long long) * d->L, cudaMemcpyDeviceToHost, st),
+       "lattice counts D2H");
+    CU(cudaStreamSynchronize(st), "lattice counts D2H");
+    for (int32_t l = 0; l < d->L; l++)
+      if (d->chan_state[l] == 1) lat_use = std::max<int64_t>(lat_use, (int64_t)n[l]);
+  }
+  const bool g_log = d->p.gc_interval == 0 && log_use > w.log_cap / 2 && w.log_cap < (int64_t)INT32_MAX / 2;
+  const bool g_lat = d->p.lattice && lat_use > w.lat_cap / 2;
+  if (!g_log && !g_lat) return WFST_OK;
+  CU(cudaStreamSynchronize(st), "stream headroom");
+  const int rc = grow_capacities(d, g_log, g_lat, false, false);
+  return rc == WFST_ERR_CAPACITY ? WFST_OK : rc;  // no room: the channels keep running until they overflow
+}
+
 static bool rec_less(const wfst_lat_record& x, const wfst_lat_record& y) {
   if (x.t != y.t) return x.t < y.t;
   if (x.src_state != y.src_state) return x.src_state < y.src_state;
@@ -918,7 +1054,7 @@ extern "C" int wfst_lattice_export(wfst_decoder* d, int32_t lane, wfst_lat_recor
   n = std::min<unsigned long long>(n, (unsigned long long)d->w.lat_cap);
   std::vector<LatRec> recs(n);
   if (n)
-    CU(cudaMemcpy(recs.data(), d->w.lat_out + (size_t)lane * d->w.lat_cap, sizeof(LatRec) * n,
+    CU(cudaMemcpy(recs.data(), d->w.lat_out + (size_t)lane * d->w.lat_stride, sizeof(LatRec) * n,
                   cudaMemcpyDeviceToHost),
        "lattice D2H");
   std::vector<wfst_lat_record> o(n);
@@ -1028,6 +1164,8 @@ extern "C" int wfst_stream_advance(wfst_decoder* d, const int32_t* channels, int
     d->h_calls[channels[i]] = LaneCall{i, chunk_lens[i], want_partial ? kCallPartial : 0, -1};
   rc = run_call(d, lp, dtype, stride_b, stride_t, st, want_partial ? words_cap : 1);
   if (rc != WFST_OK) return rc;
+  rc = stream_headroom(d, st);
+  if (rc != WFST_OK) return rc;
   for (int32_t i = 0; i < n; i++) {
     d->chan_t[channels[i]] += chunk_lens[i];
     if (want_partial) {
@@ -1100,8 +1238,9 @@ extern "C" int wfst_test_barrier_timeout(wfst_decoder* d, int64_t timeout_ns) {
 extern "C" int wfst_mem_stats(wfst_decoder* d, int64_t* out, int32_t n) {
   if (!d || !out || n < 0) return fail(WFST_ERR_INVALID_ARG, "mem_stats: bad argument");
   std::lock_guard<std::mutex> lock(d->mu);
-  const int64_t v[WFST_MEM_COUNT] = {d->bytes, d->w.qcap, d->w.log_cap, d->w.lat_cap, d->w.path_cap, d->grows,
-                                     d->max_frames};
+  const int64_t lazy = lazy_committed(d);
+  const int64_t v[WFST_MEM_COUNT] = {d->bytes + lazy, d->w.qcap, d->w.log_cap, d->w.lat_cap, d->w.path_cap, d->grows,
+                                     d->max_frames, lazy_reserved(d), lazy};
   for (int32_t i = 0; i < n && i < WFST_MEM_COUNT; i++) out[i] = v[i];
   return WFST_OK;
 }

@@ -128,6 +128,10 @@ struct DevWork {
   int32_t L, N;
   int64_t qcap;                   // frontier capacity per lane per frame
   int64_t log_cap, lat_cap, path_cap;
+  // distance in entries between consecutive lanes' regions of the front /
+  // score / worklist, winners-log / bwd and lattice arrays: the reserved
+  // size, at least the capacity (lazily committed regions, §6.2)
+  int64_t q_stride, log_stride, lat_stride;
   int64_t tiles_cap;              // tiles per lane per frame
   int32_t lattice, max_frames;
   ulonglong2* ent;                // [L][N][2] recombination entries, 16 bytes per state and frame

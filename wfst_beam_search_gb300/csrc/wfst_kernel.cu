@@ -325,7 +325,7 @@ __device__ __forceinline__ size_t pl(const DevWork& w, int par, int l) {
   return ((size_t)par * w.L + l) * (size_t)w.N;       // per-state arrays of a lane (marks)
 }
 __device__ __forceinline__ size_t ql(const DevWork& w, int par, int l) {
-  return ((size_t)par * w.L + l) * (size_t)w.qcap;    // front / score / worklists
+  return ((size_t)par * w.L + l) * (size_t)w.q_stride;  // front / score / worklists
 }
 __device__ __forceinline__ size_t tl(const DevWork& w, int par, int l) {
   return ((size_t)par * w.L + l) * (size_t)w.tiles_cap;
@@ -397,7 +397,7 @@ __device__ __forceinline__ int32_t wlog_delta(const RunArgs& a, int32_t x) {
   return a.gc_interval > 0 ? sext30((uint32_t)x) : x;
 }
 __device__ __forceinline__ int2* wlog_at(const DevWork& w, int l, int64_t i) {
-  return w.wlog + (size_t)l * (size_t)w.log_cap + (size_t)((unsigned long long)i & w.log_mask);
+  return w.wlog + (size_t)l * (size_t)w.log_stride + (size_t)((unsigned long long)i & w.log_mask);
 }
 // The winners-log entry of a frame token: its arc and the distance back to
 // the token it came from (0 for the start token).
@@ -530,7 +530,7 @@ __device__ __forceinline__ unsigned long long warp_lat_reserve(const RunArgs& a,
 }
 __device__ __forceinline__ void lat_put(const RunArgs& a, int l, unsigned long long p, const LatRec& r) {
   const DevWork& w = a.w;
-  if (p < (unsigned long long)w.lat_cap) w.lat[(size_t)l * w.lat_cap + p] = r;
+  if (p < (unsigned long long)w.lat_cap) w.lat[(size_t)l * w.lat_stride + p] = r;
   else lane_ovf(a, l, kOvfArena);
 }
 
@@ -1087,7 +1087,7 @@ __device__ void init_lane_global(const RunArgs& a, int l) {
   const int4 m = __ldg(g.meta + s0);
   const uint32_t deg = (uint32_t)(m.y - m.x);
   *ent_at(w, l, s0, 0) = make_ulonglong2(mk_key(0.0f, -1), 0ull);
-  *tpos_at(w, l, s0, 0) = 0;
+  if (tpos_kept(a)) *tpos_at(w, l, s0, 0) = 0;
   *reinterpret_cast<int4*>(w.front + ql(w, 0, l)) = make_int4(s0, 0, m.x, m.w);
   if (deg > 0)
     for (uint32_t k = 0; k <= (deg - 1) / kTile; k++) w.tile_first[tl(w, 0, l) + k] = 0;
@@ -1183,11 +1183,11 @@ __device__ bool bwd_sweep(const RunArgs& a, Smem& S, unsigned& epoch, bool final
       for (int gi = (int)gstart; gi < gtotal; gi += (int)gstride) {
         const int l = find_lane(S.pre_e, L, gi);
         const int64_t r = S.glo[l] + (gi - S.pre_e[l]);
-        const LatRec rec = w.lat[(size_t)l * w.lat_cap + r];
+        const LatRec rec = w.lat[(size_t)l * w.lat_stride + r];
         const int flags = rec.frame_flags & 15;
         if (flags & kRecDead) continue;
         if (kk >= 0 && (((flags & kRecEps) != 0) != eps_group)) continue;
-        uint32_t* bw = w.bwd + (size_t)l * w.log_cap;
+        uint32_t* bw = w.bwd + (size_t)l * w.log_stride;
         const float bd = rec.dst_tok < 0 ? 0.0f : unord_f(__ldcg(bw + rec.dst_tok));
         const unsigned ov = ord_f(__fadd_rn(rec.arcscore, bd));
         const unsigned old = atomicMax(bw + rec.src_tok, ov);
@@ -1213,7 +1213,7 @@ __device__ bool lattice_prune(const RunArgs& a, Smem& S, unsigned& epoch) {
     const SmLane& s = S.lane[l];
     if (!s.closure) continue;
     const int64_t n = min(s.cursor, w.log_cap);
-    uint32_t* bw = w.bwd + (size_t)l * w.log_cap;
+    uint32_t* bw = w.bwd + (size_t)l * w.log_stride;
     for (int64_t i = gstart; i < n; i += gstride) bw[i] = ord_f(-INFINITY);
   }
   if (!bwd_sweep(a, S, epoch, true)) return false;
@@ -1224,8 +1224,8 @@ __device__ bool lattice_prune(const RunArgs& a, Smem& S, unsigned& epoch) {
     if (!s.closure) continue;
     const float thr = __fsub_rn(__ldcg(&w.res[l].score), a.output_beam);
     const int64_t hi = (int64_t)min(__ldcg(&w.lat_cnt[l]), (unsigned long long)w.lat_cap);
-    const LatRec* R = w.lat + (size_t)l * w.lat_cap;
-    const uint32_t* bw = w.bwd + (size_t)l * w.log_cap;
+    const LatRec* R = w.lat + (size_t)l * w.lat_stride;
+    const uint32_t* bw = w.bwd + (size_t)l * w.log_stride;
     for (int64_t base = (int64_t)blockIdx.x * kThreads + (tid & ~31); base < hi; base += gstride) {
       const int64_t r = base + lane;
       bool keep = false;
@@ -1243,7 +1243,7 @@ __device__ bool lattice_prune(const RunArgs& a, Smem& S, unsigned& epoch) {
         unsigned long long b = 0;
         if (lane == ld) b = atomicAdd(&w.lat_out_n[l], (unsigned long long)__popc(m));
         b = __shfl_sync(0xffffffffu, b, ld);
-        if (keep) w.lat_out[(size_t)l * w.lat_cap + b + __popc(m & lanemask_lt())] = rec;
+        if (keep) w.lat_out[(size_t)l * w.lat_stride + b + __popc(m & lanemask_lt())] = rec;
       }
     }
   }
@@ -1287,8 +1287,8 @@ __device__ bool interval_prune(const RunArgs& a, Smem& S, unsigned& epoch) {
     if (!s.closure) continue;
     const int64_t* B = w.lat_groups + (size_t)l * mf;
     const int64_t lo = s.res_hi < 0 ? 0 : B[s.res_hi], hi = B[s.t];
-    const LatRec* R = w.lat + (size_t)l * w.lat_cap;
-    uint32_t* bw = w.bwd + (size_t)l * w.log_cap;
+    const LatRec* R = w.lat + (size_t)l * w.lat_stride;
+    uint32_t* bw = w.bwd + (size_t)l * w.log_stride;
     for (int64_t r = lo + gstart; r < hi; r += gstride) {
       const LatRec rec = R[r];
       if (rec.frame_flags & kRecDead) continue;
@@ -1304,7 +1304,7 @@ __device__ bool interval_prune(const RunArgs& a, Smem& S, unsigned& epoch) {
     const SmLane& s = S.lane[l];
     if (!s.closure) continue;
     const int par = s.t & 1;
-    uint32_t* bw = w.bwd + (size_t)l * w.log_cap;
+    uint32_t* bw = w.bwd + (size_t)l * w.log_stride;
     for (int64_t p = gstart; p < s.n_cur; p += gstride) {
       const int32_t st = __ldcg(&w.front[ql(w, par, l) + p].state);
       const float sc = key_score(__ldcg(&ent_at(w, l, st, par)->x));
@@ -1322,8 +1322,8 @@ __device__ bool interval_prune(const RunArgs& a, Smem& S, unsigned& epoch) {
     const float lim = -__fadd_rn(__fadd_rn(a.output_beam, 1.0f), __fmul_rn(0x1p-12f, fabsf(M)));
     const int64_t* B = w.lat_groups + (size_t)l * mf;
     const int64_t lo = s.res_hi < 0 ? 0 : B[s.res_hi], hi = B[s.t];
-    LatRec* R = w.lat + (size_t)l * w.lat_cap;
-    const uint32_t* bw = w.bwd + (size_t)l * w.log_cap;
+    LatRec* R = w.lat + (size_t)l * w.lat_stride;
+    const uint32_t* bw = w.bwd + (size_t)l * w.log_stride;
     for (int64_t r = lo + gstart; r < hi; r += gstride) {
       const LatRec rec = R[r];
       bool keep = false;
@@ -1366,8 +1366,8 @@ __device__ bool interval_prune(const RunArgs& a, Smem& S, unsigned& epoch) {
     if (!s.closure) continue;
     const int64_t lo = s.res_hi < 0 ? 0 : w.lat_groups[(size_t)l * mf + s.res_hi];  // unchanged by (5)
     const int64_t hi = s.res_lo;
-    const LatRec* R = w.lat + (size_t)l * w.lat_cap;
-    LatRec* O = w.lat_out + (size_t)l * w.lat_cap;
+    const LatRec* R = w.lat + (size_t)l * w.lat_stride;
+    LatRec* O = w.lat_out + (size_t)l * w.lat_stride;
     unsigned long long* cur = reinterpret_cast<unsigned long long*>(w.lat_gtmp) + (size_t)l * mf;
     for (int64_t r = lo + gstart; r < hi; r += gstride) {
       const LatRec rec = R[r];
@@ -1384,8 +1384,8 @@ __device__ bool interval_prune(const RunArgs& a, Smem& S, unsigned& epoch) {
     if (!s.closure) continue;
     const int64_t* B = w.lat_groups + (size_t)l * mf;
     const int64_t lo = s.res_hi < 0 ? 0 : B[s.res_hi], hi = B[s.t];
-    LatRec* R = w.lat + (size_t)l * w.lat_cap;
-    const LatRec* O = w.lat_out + (size_t)l * w.lat_cap;
+    LatRec* R = w.lat + (size_t)l * w.lat_stride;
+    const LatRec* O = w.lat_out + (size_t)l * w.lat_stride;
     for (int64_t r = lo + gstart; r < hi; r += gstride) R[r] = O[r - lo];
   }
   return grid_sync(a, S, epoch);
@@ -1697,7 +1697,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         const int l = find_lane(S.pre_d, L, gi);
         const SmLane& s = S.lane[l];
         const int64_t r = s.res_lo + (gi - S.pre_d[l]);
-        LatRec* rp = w.lat + (size_t)l * w.lat_cap + r;
+        LatRec* rp = w.lat + (size_t)l * w.lat_stride + r;
         LatRec rec = *rp;
         const int par = s.t & 1;
         const int64_t base_new = s.cursor;  // frame t
@@ -1798,7 +1798,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
           r.end = __fadd_rn(score, fw);
           r.arcscore = fw;
           const unsigned long long pos = atomicAdd(&w.lat_cnt[l], 1ull);
-          if (pos < (unsigned long long)w.lat_cap) w.lat[(size_t)l * w.lat_cap + pos] = r;
+          if (pos < (unsigned long long)w.lat_cap) w.lat[(size_t)l * w.lat_stride + pos] = r;
           else lane_ovf(a, l, kOvfArena);
         }
       }
@@ -1915,7 +1915,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
             r.end = score;
             r.arcscore = 0.f;
             const unsigned long long pos = atomicAdd(&w.lat_cnt[l], 1ull);
-            if (pos < (unsigned long long)w.lat_cap) w.lat[(size_t)l * w.lat_cap + pos] = r;
+            if (pos < (unsigned long long)w.lat_cap) w.lat[(size_t)l * w.lat_stride + pos] = r;
             else lane_ovf(a, l, kOvfArena);
           }
         }

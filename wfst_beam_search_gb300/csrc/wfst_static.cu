@@ -125,6 +125,9 @@ size_t layout(unsigned char* base, const DevGraph& G, int L, int T, int64_t log_
   w.log_cap = log_cap;
   w.log_mask = ~0ull;  // a flat log (no winners-log GC here)
   w.lat_cap = 0;
+  w.q_stride = w.qcap;  // flat tables: one lane's region after another
+  w.log_stride = w.log_cap;
+  w.lat_stride = 0;
   w.path_cap = 4 * mf * (1 + (int64_t)G.eps_depth);
   w.tiles_cap = G.A / kTile + 2;
   w.lattice = 0;
