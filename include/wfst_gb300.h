@@ -304,7 +304,8 @@ int wfst_stream_release(wfst_decoder* d, int32_t channel);
  * at the second barrier */
 #define WFST_STAT_NS_PROLOGUE 15
 #define WFST_STAT_LAT_HELD 23     /* lattice records held in the arenas of the call's lanes at its end */
-#define WFST_STAT_COUNT 24
+#define WFST_STAT_EPS_PASSES 24   /* epsilon-closure worklist passes (each ends at a grid barrier) */
+#define WFST_STAT_COUNT 25
 int wfst_stats(wfst_decoder* d, int64_t* out, int32_t n);
 
 /*

@@ -740,6 +740,7 @@ static int run_call(wfst_decoder* d, const void* lp, int32_t dtype, int64_t stri
     S[WFST_STAT_LAT_HELD] += (int64_t)x.lat_held;
   }
   S[WFST_STAT_BARRIERS] = d->h_bar->epochs;
+  S[WFST_STAT_EPS_PASSES] = d->h_bar->eps_passes;
   S[WFST_STAT_KERNEL_NS] = (int64_t)(ms * 1e6);
   S[WFST_STAT_NS_INIT] = (int64_t)d->h_prof[kProfInit];
   S[WFST_STAT_NS_MAX] = (int64_t)d->h_prof[kProfCommitMax];

@@ -114,7 +114,7 @@ struct GridBar {
   unsigned int error;             // 1 = barrier timeout, 2 = closure did not converge
   unsigned int epochs;            // barriers executed (written at the end)
   unsigned int changed[3];        // per-pass change flags (lattice epsilon groups)
-  unsigned int pad;
+  unsigned int eps_passes;        // epsilon-closure worklist passes run (written at the end)
 };
 
 struct TokRec {                   // a frontier token (or epsilon worklist entry), 16 bytes

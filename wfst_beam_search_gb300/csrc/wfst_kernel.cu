@@ -94,6 +94,7 @@ struct Smem {
   float bt_score;
   unsigned long long gc_min;      // GC round: deepest anchor-chain depth another chain met
   int32_t gc_ok, gc_nw;
+  unsigned eps_passes;            // epsilon-closure worklist passes of this launch
 };
 
 // ------------------------------------------------------------------ helpers
@@ -908,6 +909,7 @@ __device__ bool run_closure(const RunArgs& a, Smem& S, unsigned& epoch) {
     if (blockIdx.x == 0)
       for (int l = tid; l < L; l += kThreads)
         if (S.lane[l].closure) w.wl_cnt[(size_t)zero_slot * L + l] = 0ull;
+    if (tid == 0) S.eps_passes++;
     eps_tiles(a, S, buf, next_slot);
     __syncthreads();
     for (int l = tid; l < L; l += kThreads)
@@ -1435,6 +1437,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
   unsigned long long* prof = S.prof;
   if (tid < kProfSlots) prof[tid] = 0;
   if (tid < 2) S.tctr[tid] = 0u;
+  if (tid == 0) S.eps_passes = 0u;
   if (tid == 0) prof[kProfSlots] = prof[kProfSlots + 1] = gtimer();
   const int tlast = 0, tsub = 1;
 
@@ -2080,6 +2083,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     }
     if (tid == 0) {
       w.bar->epochs = epoch;
+      w.bar->eps_passes = S.eps_passes;
       prof_mark(prof, tlast, kProfTail);
       for (int i = 0; i < kProfSlots; i++) w.prof[i] = prof[i];
     }
