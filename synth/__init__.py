@@ -12,6 +12,9 @@ Workloads (one per decoding regime the GPU WFST decoder page covers):
   3 tlg       B=32,  T=300, V=5000, 1M states / 6M arcs, 20% epsilon arcs, fp32
   4 stream    128 lanes, T<=800 in 16-frame chunks, workload 2's graph, fp16,
               lattice on
+  5 hlg_zipf15  workload 2 with the degree law taken literally: non-blank
+              out-degree Zipf(s = 1.5) capped at 2000 (mean 34.3, ~70M arcs
+              on 2M states), reported beside workload 2 as a stress case
 
 Graph conventions (the decoder's C ABI):
   * CSR by source state: ``row_splits`` int64 [N+1], per-arc ``ilabel`` int32
@@ -86,6 +89,11 @@ WORKLOADS = {
                 search_beam=16.0, output_beam=10.0, min_active=200, max_active=10_000,
                 lattice=True, streaming=True, chunk=16,
                 graph=dict(kind="same_as", of=2)),
+    5: Workload(5, "hlg_zipf15", B=64, T=500, V=5000, dtype="f16", seed=5,
+                search_beam=20.0, output_beam=8.0, min_active=200, max_active=10_000,
+                lattice=False,
+                graph=dict(kind="zipf", N=2_000_000, s=1.5, cap=2000,
+                           word_max=200_000, p_word=0.1, w_kind="exp")),
 }
 
 
@@ -222,13 +230,16 @@ def make_graph(i: int) -> dict:
         elif spec["kind"] == "poisson":
             deg = rng.poisson(spec["lam"], size=N).astype(np.int64)
         else:
-            s = zipf_exponent(spec["mean_nb"], spec["cap"])
+            # the exponent as given, or solved for the requested mean (and the
+            # total then trimmed to the requested arc count)
+            s = spec["s"] if "s" in spec else zipf_exponent(spec["mean_nb"], spec["cap"])
             k = np.arange(1, spec["cap"] + 1, dtype=np.float64)
             cdf = np.cumsum(k ** (-s))
             cdf /= cdf[-1]
             deg = np.searchsorted(cdf, rng.random(N), side="right").astype(np.int64) + 1
             deg = np.minimum(deg, spec["cap"])
-            deg = _fit_total(deg, spec["A"] - N, 1, spec["cap"])
+            if "A" in spec:
+                deg = _fit_total(deg, spec["A"] - N, 1, spec["cap"])
         n_nb = int(deg.sum())
         nb_src = np.repeat(np.arange(N, dtype=np.int64), deg)
         nb_dst = rng.integers(0, N, size=n_nb).astype(np.int32)
