@@ -117,6 +117,38 @@ def algorithmic_bytes(st, V, esz):
             + BYTES_M * st["sum_m"] + st["frames"] * V * esz)
 
 
+def random_accesses(st):
+    """Random line accesses of a decode that its data layout cannot avoid:
+    per frontier token its recombination entry and its arc row, per admitted
+    candidate the destination's entry, per epsilon arc relaxed the source's
+    arc row and the destination's entry."""
+    return 2 * st["sum_n"] + st["sum_a"] + 2 * st["eps"]
+
+
+def random_access_ceiling(W, torch, dev, stream, table_bytes=1 << 32, reps=3):
+    """Best rate of random 16-byte and 64-byte reads from a 4 GiB table (the
+    library's measurement kernel wfst_probe_random_gather), reads per
+    second, timed with CUDA events on `stream`."""
+    table = torch.ones(table_bytes // 4, dtype=torch.int32, device=dev)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    grid, loads = 8 * sms, 256
+    best = 0.0
+    for seg in (16, 64):
+        for rep in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            W.wfst_probe_random_gather(W._ptr(table), table_bytes, seg, grid, loads, rep, W._ptr(sink),
+                                       W._stream(stream))
+            e1.record(stream)
+            e1.synchronize()
+            reads = grid * 512 // (seg // 16) * loads
+            best = max(best, reads / (e0.elapsed_time(e1) / 1e3))
+    del table
+    return best
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -440,6 +472,15 @@ def run_gpu(args):
     peak, peak_kind = load_peaks()
     achieved = alg / kmean_s / 1e9
     res_ok = int(meta[:, 0].sum())
+    ra = None
+    if not args.no_probe:
+        ceil_ = random_access_ceiling(W, torch, dev, stream)
+        acc = random_accesses(st0)
+        ra = {"accesses": int(acc), "achieved_per_s": acc / kmean_s, "ceiling_per_s": ceil_,
+              "frac": acc / kmean_s / ceil_,
+              "counted": "2 per frontier token (recombination entry, arc row) + 1 per admitted candidate "
+                         "(destination entry) + 2 per epsilon arc relaxed",
+              "ceiling": "random 16-B / 64-B reads of a 4 GiB table (wfst_probe_random_gather), best of 3"}
     h2d = int(lp_host.nbytes + lens_np.nbytes + 16 * B)
     d2h = int(B * (32 + 64 + 64) + 32 + B * words_cap * 4)
     cpu = None
@@ -459,6 +500,7 @@ def run_gpu(args):
                      "peak_kind": peak_kind, "traffic_unit": "bytes per launch",
                      "kernel": "decode_kernel", "kernel_ms": kmean_s * 1e3,
                      "algorithmic_bytes": int(alg)},
+        "random_access": ra,
         "e2e": {"value": job_rate(job_frames, e2e_s), "unit": "frames/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "phases_ms": {k[3:]: st0[k] / 1e6 for k in ("ns_init", "ns_max", "ns_expand", "ns_closure",
@@ -490,6 +532,7 @@ def main():
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-probe", action="store_true", help="skip the random-read ceiling measurement")
     ap.add_argument("--lanes", type=int, default=0, help="lanes per rank (default: the workload's B)")
     ap.add_argument("--no-ub-skip", action="store_true", help="turn off the exact upper-bound skips")
     ap.add_argument("--frontier-cap", type=int, default=0, help="tokens per lane per frame (0: default)")

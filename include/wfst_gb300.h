@@ -347,6 +347,20 @@ int wfst_mem_stats(wfst_decoder* d, int64_t* out, int32_t n);
 int wfst_test_barrier_timeout(wfst_decoder* d, int64_t timeout_ns);
 
 /*
+ * A measurement kernel, not part of the decoder (the page has no
+ * counterpart): reads random seg_bytes-long segments (16, 64 or 128 bytes,
+ * segment-aligned) of the caller's device table, grid CTAs of 512 threads,
+ * loads_per_thread reads per thread (a multiple of 4, issued four at a
+ * time).  Timed by the caller on `stream`, it gives the device's ceiling for
+ * random reads per second, the limit of the decoder's own random line
+ * accesses.  table: device, 16-byte aligned, table_bytes / seg_bytes in
+ * [1, 2^32); sink: a device int32 the kernel practically never writes.
+ * Errors: INVALID_ARG, CUDA (launch).
+ */
+int wfst_probe_random_gather(const void* table, int64_t table_bytes, int32_t seg_bytes, int32_t grid,
+                             int32_t loads_per_thread, int32_t seed, int32_t* sink, void* stream);
+
+/*
  * Offline decode that allocates nothing (no device or pinned memory, no
  * decoder object).  The web page "GPU WFST Beam-Search Decoder" has no
  * counterpart for it.  This is the same decode as wfst_decode for callers

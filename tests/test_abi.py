@@ -66,6 +66,7 @@ def test_last_error_and_argument_checks_without_gpu(lib):
                lib.wfst_stats(None, None, 0),
                lib.wfst_mem_stats(None, None, 0),
                lib.wfst_test_barrier_timeout(None, 200_000_000),
+               lib.wfst_probe_random_gather(None, 0, 16, 1, 4, 0, None, None),
                lib.wfst_decoder_create(None, None, 1, 1, None, None)):
         assert rc == -1
         assert lib.wfst_last_error()

@@ -37,7 +37,7 @@ EXPORTED = ["wfst_graph_upload", "wfst_graph_info", "wfst_graph_free", "wfst_dec
             "wfst_decoder_free", "wfst_decode", "wfst_lattice_export", "wfst_stream_create",
             "wfst_stream_advance", "wfst_stream_finalize", "wfst_stream_release", "wfst_stats",
             "wfst_decode_static", "wfst_mem_stats", "wfst_blank_skip", "wfst_test_barrier_timeout",
-            "wfst_last_error"]
+            "wfst_probe_random_gather", "wfst_last_error"]
 
 
 class WfstError(RuntimeError):
@@ -107,6 +107,7 @@ def load(build_if_missing: bool = False):
         L.wfst_stats.argtypes = [P, P, i32]
         L.wfst_mem_stats.argtypes = [P, P, i32]
         L.wfst_test_barrier_timeout.argtypes = [P, i64]
+        L.wfst_probe_random_gather.argtypes = [P, i64, i32, i32, i32, i32, P, P]
         L.wfst_blank_skip.argtypes = [P, i32, i64, i64, i32, i32, C.c_float, P, i32, i32, P, P, P, P]
         for name in EXPORTED:
             if name not in ("wfst_last_error", "wfst_graph_free", "wfst_decoder_free"):
@@ -228,6 +229,11 @@ def wfst_stats(h):
 
 def wfst_test_barrier_timeout(h, timeout_ns):
     _check(load().wfst_test_barrier_timeout(h, int(timeout_ns)))
+
+
+def wfst_probe_random_gather(table, table_bytes, seg_bytes, grid, loads_per_thread, seed, sink, stream):
+    _check(load().wfst_probe_random_gather(table, table_bytes, seg_bytes, grid, loads_per_thread, seed, sink,
+                                           stream))
 
 
 def wfst_mem_stats(h):

@@ -1,6 +1,6 @@
 """Compile the CUDA decoder library for GB300 (sm_103a), in tree.
 
-Five translation units are compiled in parallel and linked into
+Six translation units are compiled in parallel and linked into
 ``wfst_beam_search_gb300/_build/libwfst_gb300.so``.
 """
 from __future__ import annotations
@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libwfst_gb300.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["wfst_kernel.cu", "wfst_api.cu", "wfst_static.cu", "wfst_preslice.cu", "wfst_vmm.cu"]
+SOURCES = ["wfst_kernel.cu", "wfst_api.cu", "wfst_static.cu", "wfst_preslice.cu", "wfst_vmm.cu", "wfst_probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
