@@ -509,6 +509,7 @@ def run_gpu(args):
                                                      "ns_final", "ns_wait_y")},
         "steps_per_decode": st0["steps"], "barriers_per_decode": st0["barriers"],
         "eps_passes_per_decode": st0["eps_passes"],
+        "log_high_water": st0["log_high_water"],
         "gpu_launches": args.steps * calls_per_step,
         "lanes_ok": res_ok,
         "lanes_overflowed": int((meta[:, 2] != 0).sum()),   # capacity bits left after growth (0 expected)

@@ -305,7 +305,8 @@ int wfst_stream_release(wfst_decoder* d, int32_t channel);
 #define WFST_STAT_NS_PROLOGUE 15
 #define WFST_STAT_LAT_HELD 23     /* lattice records held in the arenas of the call's lanes at its end */
 #define WFST_STAT_EPS_PASSES 24   /* epsilon-closure worklist passes (each ends at a grid barrier) */
-#define WFST_STAT_COUNT 25
+#define WFST_STAT_LOG_HW 25       /* most winners-log entries any lane held live during the call */
+#define WFST_STAT_COUNT 26
 int wfst_stats(wfst_decoder* d, int64_t* out, int32_t n);
 
 /*

@@ -26,7 +26,8 @@ REC_EPS, REC_FINAL, REC_REDIRECT = 1, 2, 4
 STAT_NAMES = ["frames", "arcs_expanded", "sum_n", "sum_D", "sum_a", "sum_m", "eps",
               "steps", "barriers", "kernel_ns", "ns_init", "ns_max", "ns_expand", "ns_closure",
               "ns_prune", "ns_prologue", "ns_commit", "ns_clear", "ns_max_tiles", "ns_wait_x",
-              "ns_expand_tiles", "ns_final", "ns_wait_y", "lattice_records_held", "eps_passes"]
+              "ns_expand_tiles", "ns_final", "ns_wait_y", "lattice_records_held", "eps_passes",
+              "log_high_water"]
 ERRORS = {-1: "INVALID_ARG", -2: "CORRUPT_GRAPH", -3: "CUDA", -4: "OOM", -5: "CAPACITY",
           -6: "TIMEOUT", -7: "STATE"}
 

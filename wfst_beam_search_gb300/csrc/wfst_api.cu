@@ -293,6 +293,7 @@ struct wfst_decoder {
   // lazily committed tables (§6.2): worst-case address ranges, physical
   // memory for the current capacities only; growth maps more after it
   LazyRegions lz_front, lz_score, lz_wl;   // [2][L] regions, one stride (entries)
+  LazyRegions lz_anc;                      // [2][L], the same stride: ancestor GC (epsilon-free graphs)
   LazyRegions lz_log, lz_bwd;              // [L] regions, one stride
   LazyRegions lz_lat, lz_lat_out;          // [L] regions, one stride
 };
@@ -304,6 +305,7 @@ static void sync_lazy(wfst_decoder* d) {
   w.front = static_cast<TokRec*>(d->lz_front.base());
   w.score = static_cast<float*>(d->lz_score.base());
   w.wl = d->lz_wl.active() ? static_cast<TokRec*>(d->lz_wl.base()) : nullptr;
+  w.anc = d->lz_anc.active() ? static_cast<int32_t*>(d->lz_anc.base()) : nullptr;
   w.q_stride = d->lz_front.stride_entries();
   w.wlog = static_cast<int2*>(d->lz_log.base());
   w.bwd = d->lz_bwd.active() ? static_cast<uint32_t*>(d->lz_bwd.base()) : nullptr;
@@ -314,7 +316,8 @@ static void sync_lazy(wfst_decoder* d) {
 }
 
 static int64_t lazy_committed(const wfst_decoder* d) {
-  const LazyRegions* r[] = {&d->lz_front, &d->lz_score, &d->lz_wl, &d->lz_log, &d->lz_bwd, &d->lz_lat, &d->lz_lat_out};
+  const LazyRegions* r[] = {&d->lz_front, &d->lz_score, &d->lz_wl, &d->lz_anc, &d->lz_log, &d->lz_bwd, &d->lz_lat,
+                            &d->lz_lat_out};
   int64_t b = 0;
   for (const LazyRegions* x : r)
     if (x->active()) b += (int64_t)x->committed_bytes();
@@ -322,7 +325,8 @@ static int64_t lazy_committed(const wfst_decoder* d) {
 }
 
 static int64_t lazy_reserved(const wfst_decoder* d) {
-  const LazyRegions* r[] = {&d->lz_front, &d->lz_score, &d->lz_wl, &d->lz_log, &d->lz_bwd, &d->lz_lat, &d->lz_lat_out};
+  const LazyRegions* r[] = {&d->lz_front, &d->lz_score, &d->lz_wl, &d->lz_anc, &d->lz_log, &d->lz_bwd, &d->lz_lat,
+                            &d->lz_lat_out};
   int64_t b = 0;
   for (const LazyRegions* x : r)
     if (x->active()) b += (int64_t)x->reserved_bytes();
@@ -404,6 +408,7 @@ static void decoder_destroy(wfst_decoder* d) {
     d->lz_front.release();
     d->lz_score.release();
     d->lz_wl.release();
+    d->lz_anc.release();
     d->lz_log.release();
     d->lz_bwd.release();
     d->lz_lat.release();
@@ -505,17 +510,18 @@ extern "C" int wfst_decoder_create(wfst_graph* g, const wfst_params* params, int
     d->lz_front.init(g->device, 2 * max_lanes, sizeof(TokRec), q_align);
     d->lz_score.init(g->device, 2 * max_lanes, sizeof(float), q_align);
     if (G.has_eps) d->lz_wl.init(g->device, 2 * max_lanes, sizeof(TokRec), q_align);
+    if (gc && !G.has_eps) d->lz_anc.init(g->device, 2 * max_lanes, sizeof(int32_t), q_align);
     d->lz_log.init(g->device, max_lanes, sizeof(int2), log_align);
     if (params->lattice) {
       d->lz_bwd.init(g->device, max_lanes, sizeof(uint32_t), log_align);
       d->lz_lat.init(g->device, max_lanes, sizeof(LatRec), lat_align);
       d->lz_lat_out.init(g->device, max_lanes, sizeof(LatRec), lat_align);
     }
-    LazyRegions* qg[] = {&d->lz_front, &d->lz_score, &d->lz_wl};
+    LazyRegions* qg[] = {&d->lz_front, &d->lz_score, &d->lz_wl, &d->lz_anc};
     LazyRegions* lg[] = {&d->lz_log, &d->lz_bwd};
     LazyRegions* ag[] = {&d->lz_lat, &d->lz_lat_out};
     const int64_t log_bound = gc ? kMaxGcRing : (int64_t)INT32_MAX - 1;
-    int rc = lazy_commit(qg, 3, qcap, N);
+    int rc = lazy_commit(qg, 4, qcap, N);
     if (rc == WFST_OK) rc = lazy_commit(lg, 2, log_cap, std::min<int64_t>(8 * log_cap, log_bound));
     if (rc == WFST_OK && params->lattice) rc = lazy_commit(ag, 2, lat_cap, 8 * lat_cap);
     if (rc != WFST_OK) {
@@ -738,6 +744,7 @@ static int run_call(wfst_decoder* d, const void* lp, int32_t dtype, int64_t stri
     S[WFST_STAT_ARCS] += (int64_t)(x.sum_d + x.eps + x.finals);
     S[WFST_STAT_STEPS] = std::max<int64_t>(S[WFST_STAT_STEPS], (int64_t)x.steps);
     S[WFST_STAT_LAT_HELD] += (int64_t)x.lat_held;
+    S[WFST_STAT_LOG_HW] = std::max<int64_t>(S[WFST_STAT_LOG_HW], (int64_t)x.log_hw);
   }
   S[WFST_STAT_BARRIERS] = d->h_bar->epochs;
   S[WFST_STAT_EPS_PASSES] = d->h_bar->eps_passes;
@@ -817,8 +824,8 @@ static int grow_capacities(wfst_decoder* d, bool g_log, bool g_lat, bool g_q, bo
   }
   if (g_q && w.qcap < (int64_t)G.N) {
     const int64_t cap = std::min<int64_t>(2 * w.qcap, (int64_t)G.N);
-    LazyRegions* qg[] = {&d->lz_front, &d->lz_score, &d->lz_wl};
-    if (lazy_commit(qg, 3, cap, 0) != WFST_OK) return WFST_ERR_CAPACITY;
+    LazyRegions* qg[] = {&d->lz_front, &d->lz_score, &d->lz_wl, &d->lz_anc};
+    if (lazy_commit(qg, 4, cap, 0) != WFST_OK) return WFST_ERR_CAPACITY;
     w.qcap = cap;
     grew = true;
   }
@@ -887,7 +894,7 @@ static int grow_frames(wfst_decoder* d, int32_t T) {
 
 static void stats_add(int64_t* acc, const int64_t* s) {
   for (int i = 0; i < WFST_STAT_COUNT; i++)
-    acc[i] = (i == WFST_STAT_STEPS) ? std::max(acc[i], s[i]) : acc[i] + s[i];
+    acc[i] = (i == WFST_STAT_STEPS || i == WFST_STAT_LOG_HW) ? std::max(acc[i], s[i]) : acc[i] + s[i];
 }
 
 extern "C" int wfst_decode(wfst_decoder* d, const void* log_probs, int32_t dtype, int64_t stride_b,

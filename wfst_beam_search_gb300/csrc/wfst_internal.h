@@ -55,6 +55,8 @@ struct FrameCnt {                 // per lane, per frame (ring of 4 frames)
   unsigned int admitted;          // admitted emitting candidates of that step
   unsigned long long final_key;   // (ordered final score, 0x7fffffff - state)
   unsigned long long best_key;    // (ordered score, 0x7fffffff - arc) of the best token
+  unsigned int anc_hi;            // ancestor GC: 1 + the largest checkpoint ancestor of the frame's tokens
+  unsigned int anc_lo;            // ... 0x7fffffff - the smallest (both 0 = none committed)
 };
 
 struct LaneState {                // persistent per lane (mirrored in shared memory)
@@ -74,7 +76,8 @@ struct LaneState {                // persistent per lane (mirrored in shared mem
   int32_t gc_t;                   // frames consumed at the lane's last winners-log GC round
   int64_t floor;                  // winners-log GC root: entries below it are free (0 without GC)
   int32_t fin_n;                  // finalized words (the GC-cut prefix of the best path)
-  int32_t pad;
+  int32_t gc_c;                   // ancestor GC: the checkpoint frame
+  int64_t gc_cbase;               // ancestor GC: winners-log index of the checkpoint frame's first token
 };
 
 struct LaneCall {                 // per lane, per call
@@ -88,6 +91,7 @@ struct LaneStats {                // per lane, accumulated by the kernel (zeroed
   unsigned long long frames, sum_n, sum_d, sum_a, sum_m, eps, finals;
   unsigned long long steps;
   unsigned long long lat_held;    // lattice records in the lane's arena at the end of the call
+  unsigned long long log_hw;      // most winners-log entries live (after the last cut) in the call
 };
 
 struct LatRec {                   // 32 bytes
@@ -149,6 +153,8 @@ struct DevWork {
                                   // entry i - delta (0 = none); a ring (index & log_mask) with GC
   unsigned long long log_mask;    // log_cap - 1 with GC (log_cap a power of two), else all ones
   int32_t* fin;                   // [L][fin_cap] finalized words (GC)
+  int32_t* anc;                   // [2][L][qcap] ancestor GC (epsilon-free graphs): each token's
+                                  // ancestor among the lane's checkpoint-frame tokens (its position)
   int64_t fin_cap;
   FrameCnt* fcnt;                 // [4][L]
   LaneState* lanes;               // [L]

@@ -29,6 +29,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "wfst_internal.h"
 
 namespace wfst {
@@ -59,6 +61,10 @@ struct SmLane {
   int32_t fin_n;                  // finalized words of the lane (GC)
   int32_t gc_t;                   // frames consumed at the last GC round
   int32_t gc_due;                 // a GC round runs at the end of this step
+  int32_t gc_c;                   // ancestor GC: checkpoint frame
+  int64_t gc_cbase;               // ancestor GC: winners-log index of its first token
+  int64_t gc_e;                   // ancestor GC: the cut point of this step's round
+  int64_t log_hw;                 // most winners-log entries live (cursor - root) in this call
 };
 
 struct WStage {                   // one warp's staged tokens of its current tile
@@ -339,7 +345,8 @@ __device__ __forceinline__ FrameCnt* fc_of(const DevWork& w, int f, int l) {
 // {key, src} where key = (ordered score, 0x7fffffff - arc id) of the best
 // incoming candidate so far and src = the position of that candidate's source
 // token (in the previous frame for an emitting arc; in the same frame, with
-// bit 31 set, for an epsilon arc).  Both parities of a state share one
+// bit 31 set, for an epsilon arc); with the ancestor GC the upper half of the
+// src word carries that source token's checkpoint ancestor.  Both parities of a state share one
 // 32-byte sector, so a state that stays in the frontier keeps hitting the
 // same line frame after frame.  The token's own position lives in tpos.
 __device__ __forceinline__ ulonglong2* ent_at(const DevWork& w, int l, int32_t d, int par) {
@@ -367,9 +374,10 @@ constexpr int kCasTries = 1 << 16;  // a CAS retry only follows another thread's
 // The first attempt assumes an empty entry (the common case for a new
 // state), so a claim costs one round trip; a failed CAS returns the current
 // value and the loop continues from it.
-__device__ __forceinline__ int relax_ent(const RunArgs& a, ulonglong2* e, unsigned long long key, uint32_t src) {
+__device__ __forceinline__ int relax_ent(const RunArgs& a, ulonglong2* e, unsigned long long key,
+                                         unsigned long long srcw) {
   ulonglong2 cur = make_ulonglong2(0ull, 0ull);
-  const ulonglong2 nv = make_ulonglong2(key, (unsigned long long)src);
+  const ulonglong2 nv = make_ulonglong2(key, srcw);
   for (int it = 0; it < kCasTries; it++) {
     if (key <= cur.x) return 0;
     const ulonglong2 old = cas128(e, cur, nv);
@@ -411,6 +419,29 @@ __device__ __forceinline__ void wlog_commit(const RunArgs& a, int l, int64_t idx
   if (idx - floor < w.log_cap) __stcs(wlog_at(w, l, idx), make_int2(x, arc));
   else lane_ovf(a, l, kOvfArena);
 }
+// Ancestor GC (winners-log GC on epsilon-free graphs): every committed token
+// of frame f records the position of its ancestor among the tokens of the
+// lane's checkpoint frame C (its predecessor's position when f = C + 1, else
+// its predecessor's recorded ancestor).  A frame whose tokens all share one
+// ancestor has converged: every chain passes through that checkpoint token.
+// The winning candidate's source ancestor rides in the entry (upper half of
+// its src word), so the commit needs no read of the previous frame.
+__device__ __forceinline__ int32_t anc_of(int f, int32_t arc, unsigned long long srcw, int32_t gc_c) {
+  if (arc < 0) return 0;  // the start token
+  return (f - 1 == gc_c) ? (int32_t)(srcw & 0x7fffffffull) : (int32_t)(srcw >> 32);
+}
+__device__ __forceinline__ void anc_post(const RunArgs& a, int l, int f, int32_t amin, int32_t amax) {
+  for (int o = 16; o; o >>= 1) {
+    amin = min(amin, __shfl_xor_sync(0xffffffffu, amin, o));
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  }
+  if ((threadIdx.x & 31) == 0 && amax >= 0) {
+    FrameCnt* fc = fc_of(a.w, f, l);
+    atomicMax(&fc->anc_hi, (unsigned)(amax + 1));
+    atomicMax(&fc->anc_lo, 0x7fffffffu - (unsigned)amin);
+  }
+}
+
 // Token positions per state are kept only where something looks a state's
 // token up (epsilon worklists, lattice records); the final backtrack of other
 // graphs finds its one token by a scan of the frame.
@@ -541,7 +572,7 @@ __device__ __forceinline__ void lat_put(const RunArgs& a, int l, unsigned long l
 //   stages every token's score for MODE 1.
 // MODE 1 (expand): admission against the cutoff + recombination into the
 //   next frame.
-template <int MODE, typename LP>
+template <int MODE, typename LP, bool ANC>
 __device__ void emit_tiles(const RunArgs& a, Smem& S) {
   const DevWork& w = a.w;
   const DevGraph& g = a.g;
@@ -586,6 +617,7 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
     }
     float vmax = -INFINITY;
     uint32_t admitted = 0;
+    int32_t amin = 0x7fffffff, amax = -1;  // ancestor GC: the tile's committed tokens' ancestors
     for (int32_t c = p_lo; c < p_hi; c += kTokCap) {
       const int ntok = min(kTokCap, p_hi - c);
       __syncwarp();
@@ -616,9 +648,16 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
                 const int4 m = __ldg(g.meta + tr.state);
                 if (m.z > m.y) atomicAdd(&w.stats[l].eps, (unsigned long long)(m.z - m.y));
               }
+              if (ANC) {
+                const int32_t an = anc_of(f, arc, e.y, s.gc_c);
+                w.anc[q + p] = an;
+                amin = min(amin, an);
+                amax = max(amax, an);
+              }
             }
           } else {
             sc = __ldcg(w.score + q + c + i);
+            if (ANC) ws.tpos[i] = __ldcg(w.anc + q + c + i);  // the token's checkpoint ancestor
             // entries the max pass left (lattices, tile-boundary tokens)
             if (a.lattice || (c + i == p_lo && k > 0))
               *ent_at(w, l, tr.state, par) = make_ulonglong2(0ull, 0ull);
@@ -737,8 +776,10 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
           if (adm[j]) prefetch_l2_keep(ent_at(w, l, d[j], par ^ 1));
 #pragma unroll
         for (int j = 0; j < kSPT; j++) {
-          claim[j] = adm[j] && relax_ent(a, ent_at(w, l, d[j], par ^ 1), mk_key(end[j], id[j]),
-                                         (uint32_t)(c + ti[j])) == 2;
+          const unsigned long long srcw =
+              (unsigned long long)(uint32_t)(c + ti[j]) |
+              (ANC ? (unsigned long long)(uint32_t)ws.tpos[ti[j]] << 32 : 0ull);
+          claim[j] = adm[j] && relax_ent(a, ent_at(w, l, d[j], par ^ 1), mk_key(end[j], id[j]), srcw) == 2;
           admitted += adm[j] ? 1u : 0u;
         }
         warp_claim<kSPT>(a, claim, d, l, f + 1, true);
@@ -747,6 +788,7 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
     if (MODE == 0) {
       for (int o = 16; o; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
       if (lane == 0 && vmax > -INFINITY) atomicMax(&fc_of(w, f, l)->maxkey, ord_f(vmax));
+      if (ANC) anc_post(a, l, f, amin, amax);
     } else {
       for (int o = 16; o; o >>= 1) admitted += __shfl_xor_sync(0xffffffffu, admitted, o);
       if (lane == 0 && admitted) atomicAdd(&w.stats[l].sum_a, (unsigned long long)admitted);
@@ -924,6 +966,72 @@ __device__ bool run_closure(const RunArgs& a, Smem& S, unsigned& epoch) {
 
 // ------------------------------------------------------------------ winners-log GC
 
+// Cut lane l's winners log at entry E (the whole CTA): the words of the path
+// from the root up to E are appended to the lane's finalized words, E becomes
+// the root (arc -1, no predecessor) and the ring below it is free.  Thread 0
+// follows the chain once (one load per hop), keeping its arcs newest first in
+// the lane's path buffer; the CTA then looks their output labels up and packs
+// the words oldest first.  The kept path of the lane (partial backtracks
+// splice with it) reaches below E, so it is dropped.  Lanes whose log,
+// frontier or path overflowed are left alone, and so is an E that is not
+// above the root or a chain longer than the path buffer.
+__device__ void gc_cut(const RunArgs& a, Smem& S, int l, int64_t E) {
+  const DevWork& w = a.w;
+  const DevGraph& g = a.g;
+  const SmLane& s = S.lane[l];
+  const int tid = threadIdx.x;
+  int32_t* path = w.path + (size_t)l * (size_t)w.path_cap;
+  if (tid == 0) {
+    const int64_t root = s.floor, hi = s.cursor;
+    int n = -1;
+    if (!(__ldcg(&w.lanes[l].overflow) & (kOvfArena | kOvfKept | kOvfPath)) && E > root && E < hi) {
+      w.lanes[l].bt_top = -1;
+      w.lanes[l].bt_len = 0;
+      n = 0;
+      int64_t i = E;
+      while (i > root && i < hi) {
+        const int2 e = __ldcg(wlog_at(w, l, i));
+        if (e.y < 0) break;
+        if (n >= w.path_cap) { n = -1; break; }  // longer than the buffer: no cut
+        path[n++] = e.y;
+        i -= sext30((uint32_t)e.x);
+      }
+    }
+    S.bt_n = n;
+  }
+  __syncthreads();
+  const int n = S.bt_n;
+  if (n < 0) return;
+  // words, oldest arc first: path[n-1] .. path[0]
+  int32_t* fin = w.fin + (size_t)l * (size_t)w.fin_cap;
+  int run = s.fin_n;
+  for (int base = 0; base < n; base += kThreads) {
+    const int j = base + tid;
+    const int32_t o = j < n ? __ldg(g.c_olabel + __ldcg(path + (n - 1 - j))) : 0;
+    const unsigned bal = __ballot_sync(0xffffffffu, o != 0);
+    if ((tid & 31) == 0) S.scan_tmp[tid >> 5] = __popc(bal);
+    __syncthreads();
+    int wbase = 0, tot = 0;
+    for (int ww = 0; ww < kWarps; ww++) {
+      if (ww < (tid >> 5)) wbase += S.scan_tmp[ww];
+      tot += S.scan_tmp[ww];
+    }
+    const int pos = run + wbase + __popc(bal & lanemask_lt());
+    if (o != 0 && pos < w.fin_cap) fin[pos] = o;
+    run += tot;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    if ((int64_t)run > w.fin_cap) {
+      lane_ovf(a, l, kOvfPath);  // no room for the finalized words: no cut
+    } else {
+      *wlog_at(w, l, E) = make_int2(0, -1);
+      w.lanes[l].floor = E;
+      w.lanes[l].fin_n = run;
+    }
+  }
+}
+
 // One winners-log GC round of lane l (§6.3 "Winners-log GC", §8.1 "Per-chunk
 // GC"), run by one CTA at the end of a step.  Frame t's tokens are the
 // entries [base_cur, cursor) and every live chain passes through one of them.
@@ -1035,35 +1143,7 @@ __device__ void gc_round(const RunArgs& a, Smem& S, int l) {
   }
   __threadfence();
   __syncthreads();
-  // cut at E: the words from the root up to E are final
-  if (tid == 0 && run && S.gc_ok && S.bt_idx > root) {
-    const int64_t E = S.bt_idx;
-    int32_t nw = 0;
-    int64_t i = E;
-    for (int64_t h = 0; h <= max_hops && i >= root && i < hi; h++) {
-      const int2 e = __ldcg(wlog_at(w, l, i));
-      if (e.y < 0) break;
-      if (__ldg(g.c_olabel + e.y) != 0) nw++;
-      i -= sext30((uint32_t)e.x);
-    }
-    if ((int64_t)s.fin_n + nw > w.fin_cap) {
-      lane_ovf(a, l, kOvfPath);  // no room for the finalized words: no cut
-    } else {
-      int32_t* fin = w.fin + (size_t)l * (size_t)w.fin_cap;
-      int32_t k = s.fin_n + nw;
-      i = E;
-      for (int64_t h = 0; h <= max_hops && i >= root && i < hi; h++) {
-        const int2 e = __ldcg(wlog_at(w, l, i));
-        if (e.y < 0) break;
-        const int32_t o = __ldg(g.c_olabel + e.y);
-        if (o != 0 && k > s.fin_n) fin[--k] = o;
-        i -= sext30((uint32_t)e.x);
-      }
-      *wlog_at(w, l, E) = make_int2(0, -1);
-      w.lanes[l].floor = E;
-      w.lanes[l].fin_n = s.fin_n + nw;
-    }
-  }
+  if (run && S.gc_ok) gc_cut(a, S, l, S.bt_idx);
   __syncthreads();
 }
 
@@ -1073,7 +1153,7 @@ __device__ void init_lane_global(const RunArgs& a, int l) {
   const DevWork& w = a.w;
   const DevGraph& g = a.g;
   FrameCnt z;
-  z.cnt = 0; z.maxkey = 0; z.admitted = 0; z.final_key = 0; z.best_key = 0;
+  z.cnt = 0; z.maxkey = 0; z.admitted = 0; z.final_key = 0; z.best_key = 0; z.anc_hi = 0; z.anc_lo = 0;
   for (int r = 0; r < 4; r++) w.fcnt[(size_t)r * w.L + l] = z;
   for (int r = 0; r < 3; r++) w.wl_cnt[(size_t)r * w.L + l] = 0ull;
   if (w.lattice) {
@@ -1418,7 +1498,10 @@ __device__ inline void smem_carve(Smem& S, unsigned char* raw, int L) {
   S.glo = reinterpret_cast<int64_t*>(p);
 }
 
-template <typename LP>
+// ANC: the ancestor GC is on (the winners-log GC of an epsilon-free graph);
+// a separate instantiation, so that decodes without it carry none of its
+// registers.
+template <typename LP, bool ANC>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
@@ -1459,6 +1542,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     s.fin_n = st.fin_n;
     s.gc_t = st.gc_t;
     s.gc_due = 0;
+    s.gc_c = st.gc_c;
+    s.gc_cbase = st.gc_cbase;
+    s.gc_e = 0;
+    s.log_hw = 0;
     s.row = c.row;
     s.flags = c.row >= 0 ? c.flags : 0;
     s.phase = kNone;
@@ -1481,6 +1568,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
       s.floor = 0;
       s.fin_n = 0;
       s.gc_t = 0;
+      s.gc_c = 0;
+      s.gc_cbase = 0;
     }
     s.t0 = s.t;
     s.t_end = s.t + (c.row >= 0 ? c.nframes : 0);
@@ -1604,7 +1693,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         const SmLane& s = S.lane[l];
         if (s.phase == kEmit) {
           FrameCnt z;
-          z.cnt = 0; z.maxkey = 0; z.admitted = 0; z.final_key = 0; z.best_key = 0;
+          z.cnt = 0; z.maxkey = 0; z.admitted = 0; z.final_key = 0; z.best_key = 0; z.anc_hi = 0; z.anc_lo = 0;
           *fc_of(w, s.t + 1, l) = z;
           if (g.has_eps) w.wl_cnt[l] = 0ull;
         }
@@ -1635,12 +1724,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
           pk[k] = v[k] ? gi - S.pre_b[lk[k]] : 0;
           st[k] = v[k] ? __ldcg(&w.front[ql(w, S.lane[lk[k]].t & 1, lk[k]) + pk[k]].state) : 0;
         }
-        uint32_t src[kCB];
+        unsigned long long src[kCB];
 #pragma unroll
         for (int k = 0; k < kCB; k++) {
           const ulonglong2 e = v[k] ? __ldcg(ent_at(w, lk[k], st[k], S.lane[lk[k]].t & 1)) : make_ulonglong2(0, 0);
           key[k] = e.x;
-          src[k] = ent_src(e);
+          src[k] = e.y;
         }
 #pragma unroll
         for (int k = 0; k < kCB; k++) {
@@ -1654,11 +1743,18 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
             const int64_t base_new = s.cursor;   // frame f
             const int64_t base_old = s.base_cur; // frame f-1
             // the winner's source token: same frame for an epsilon arc, else the previous one
-            const int64_t prev = ((src[k] >> 31) ? base_new : base_old) + (src[k] & 0x7fffffffu);
+            const int64_t prev = ((src[k] >> 31) & 1ull ? base_new : base_old) + (int64_t)(src[k] & 0x7fffffffull);
             wlog_commit(a, l, base_new + pk[k], s.floor, arc, prev);
             if (g.has_eps) {
               const int4 m = __ldg(g.meta + st[k]);
               if (m.z > m.y) atomicAdd(&w.stats[l].eps, (unsigned long long)(m.z - m.y));
+            }
+            if (ANC) {
+              const int32_t an = anc_of(f, arc, src[k], s.gc_c);
+              w.anc[ql(w, f & 1, l) + pk[k]] = an;
+              FrameCnt* fc = fc_of(w, f, l);
+              atomicMax(&fc->anc_hi, (unsigned)(an + 1));
+              atomicMax(&fc->anc_lo, 0x7fffffffu - (unsigned)an);
             }
           }
           if (s.phase == kFin) {
@@ -1716,7 +1812,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
       }
     }
     prof_mark(prof, tsub, kProfClear);
-    emit_tiles<0, LP>(a, S);
+    emit_tiles<0, LP, ANC>(a, S);
     prof_mark(prof, tsub, kProfMaxTiles);
     if (!grid_sync(a, S, epoch)) return;
     prof_mark(prof, tsub, kProfBarX);
@@ -1752,12 +1848,31 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         s.base_cur = s.cursor;
         s.cursor += s.n_cur;
         s.committed = s.t;
+        s.log_hw = max(s.log_hw, s.cursor - s.floor);
       }
       s.expanded = 0;
       // winners-log GC of frame t (committed above) at the end of this step
-      s.gc_due = (a.gc_interval > 0 && s.phase == kEmit && s.n_cur > 0 && s.t + 1 - s.gc_t >= a.gc_interval)
-                     ? 1 : 0;
-      if (s.gc_due) s.gc_t = s.t + 1;
+      if (ANC) {
+        // at frames that are multiples of gc_interval (the same steps in
+        // every lane, so that the lanes' cuts run side by side), a frame
+        // whose tokens share one checkpoint ancestor is cut there; frame t
+        // is then the next checkpoint
+        s.gc_due = 0;
+        if (s.phase == kEmit && s.n_cur > 0 && s.t % a.gc_interval == 0 && s.t - s.gc_c >= a.gc_interval) {
+          const FrameCnt* fc = fc_of(w, s.t, l);
+          const unsigned hi = __ldcg(&fc->anc_hi), lo = __ldcg(&fc->anc_lo);
+          if (hi > 0u && hi - 1u == 0x7fffffffu - lo) {
+            s.gc_due = 1;
+            s.gc_e = s.gc_cbase + (int64_t)(hi - 1u);
+            s.gc_c = s.t;
+            s.gc_cbase = s.base_cur;
+          }
+        }
+      } else {
+        s.gc_due = (a.gc_interval > 0 && s.phase == kEmit && s.n_cur > 0 && s.t + 1 - s.gc_t >= a.gc_interval)
+                       ? 1 : 0;
+        if (s.gc_due) s.gc_t = s.t + 1;
+      }
       if (s.phase == kEmit) {
         const unsigned mk = __ldcg(&fc_of(w, s.t, l)->maxkey);
         s.expanded = mk != 0u;
@@ -1772,7 +1887,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     if (blockIdx.x == 0 && g.has_eps)
       for (int l = tid; l < L; l += kThreads)
         if (S.lane[l].phase == kEmit) w.wl_cnt[(size_t)1 * L + l] = 0ull;
-    emit_tiles<1, LP>(a, S);
+    emit_tiles<1, LP, ANC>(a, S);
     prof_mark(prof, tsub, kProfExpTiles);
 
     // final-arc lattice records (read the entries; cleared only after the loop)
@@ -1818,7 +1933,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         const SmLane& s = S.lane[l];
         const int f = s.t, par = f & 1;
         if (s.gc_due) {
-          gc_round(a, S, l);
+          if (ANC) {
+            gc_cut(a, S, l, s.gc_e);
+            __syncthreads();  // the CTA's next task reuses the path scan space
+          } else {
+            gc_round(a, S, l);
+          }
           continue;
         }
         if (tid == 0) {
@@ -2073,6 +2193,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
       st.eps_pass = s.eps_pass;
       st.t_eff = s.t_eff;
       st.gc_t = s.gc_t;
+      st.gc_c = s.gc_c;
+      st.gc_cbase = s.gc_cbase;
       LaneStats& ls = w.stats[l];
       ls.frames += s.frames;
       ls.sum_n += s.sum_n;
@@ -2080,6 +2202,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
       ls.sum_m += s.sum_m;
       ls.steps = steps;
       if (lat) ls.lat_held = __ldcg(&w.lat_cnt[l]);
+      ls.log_hw = (unsigned long long)s.log_hw;
     }
     if (tid == 0) {
       w.bar->epochs = epoch;
@@ -2094,46 +2217,52 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
 
 size_t smem_bytes(int L) { return smem_size(L); }
 
-template <typename LP>
+template <typename LP, bool ANC>
 static cudaError_t prepare_t() {
-  return cudaFuncSetAttribute(decode_kernel<LP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(decode_kernel<LP, ANC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)smem_size(kMaxLanes));
 }
 
-cudaError_t launch_decode(const RunArgs& a, int dtype, int grid, cudaStream_t st) {
+template <typename LP, bool ANC>
+static cudaError_t launch_t(const RunArgs& a, int grid, cudaStream_t st) {
   void* args[] = {(void*)&a};
-  const size_t sm = smem_size(a.nlanes);
-  if (dtype == 1) {
-    cudaError_t e = prepare_t<__half>();
-    if (e != cudaSuccess) return e;
-    return cudaLaunchCooperativeKernel((const void*)decode_kernel<__half>, dim3(grid), dim3(kThreads), args,
-                                       sm, st);
-  }
-  cudaError_t e = prepare_t<float>();
+  cudaError_t e = prepare_t<LP, ANC>();
   if (e != cudaSuccess) return e;
-  return cudaLaunchCooperativeKernel((const void*)decode_kernel<float>, dim3(grid), dim3(kThreads), args, sm,
-                                     st);
+  return cudaLaunchCooperativeKernel((const void*)decode_kernel<LP, ANC>, dim3(grid), dim3(kThreads), args,
+                                     smem_size(a.nlanes), st);
 }
 
-// Cooperative grid for a launch over L lanes: resident CTAs per SM x SMs.
+cudaError_t launch_decode(const RunArgs& a, int dtype, int grid, cudaStream_t st) {
+  const bool anc = a.gc_interval > 0 && a.w.anc != nullptr;
+  if (dtype == 1) return anc ? launch_t<__half, true>(a, grid, st) : launch_t<__half, false>(a, grid, st);
+  return anc ? launch_t<float, true>(a, grid, st) : launch_t<float, false>(a, grid, st);
+}
+
+template <typename LP, bool ANC>
+static cudaError_t occupancy_t(size_t sm, int* per) {
+  cudaError_t e = prepare_t<LP, ANC>();
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(per, decode_kernel<LP, ANC>, kThreads, sm);
+  return e;
+}
+
+// Cooperative grid for a launch over L lanes: resident CTAs per SM x SMs
+// (the smaller of the two instantiations, so that either fits the grid).
 cudaError_t max_grid(int dtype, int L, int* grid) {
-  int dev = 0, sms = 0, per = 0;
+  int dev = 0, sms = 0, p0 = 0, p1 = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const size_t sm = smem_size(L);
   if (dtype == 1) {
-    e = prepare_t<__half>();
-    if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, decode_kernel<__half>, kThreads, sm);
+    e = occupancy_t<__half, false>(sm, &p0);
+    if (e == cudaSuccess) e = occupancy_t<__half, true>(sm, &p1);
   } else {
-    e = prepare_t<float>();
-    if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, decode_kernel<float>, kThreads, sm);
+    e = occupancy_t<float, false>(sm, &p0);
+    if (e == cudaSuccess) e = occupancy_t<float, true>(sm, &p1);
   }
   if (e != cudaSuccess) return e;
-  *grid = per * sms;
+  *grid = std::min(p0, p1) * sms;
   return cudaSuccess;
 }
 
