@@ -119,10 +119,14 @@ def algorithmic_bytes(st, V, esz):
 
 def random_accesses(st):
     """Random line accesses of a decode that its data layout cannot avoid:
-    per frontier token its recombination entry and its arc row, per admitted
-    candidate the destination's entry, per epsilon arc relaxed the source's
-    arc row and the destination's entry."""
-    return 2 * st["sum_n"] + st["sum_a"] + 2 * st["eps"]
+    per frontier token its recombination entry and the first line of its arc
+    row, one more 128-byte line per 8 emitting arcs (16-byte records), per
+    admitted candidate the destination's entry, per epsilon arc relaxed the
+    source's arc row and the destination's entry."""
+    return 2 * st["sum_n"] + st["sum_D"] // 8 + st["sum_a"] + 2 * st["eps"]
+
+
+MAX_STATS = ("steps", "log_high_water", "lattice_records_held")   # a stream's calls combine these by maximum
 
 
 def random_access_ceiling(W, torch, dev, stream, table_bytes=1 << 32, reps=3):
@@ -243,7 +247,7 @@ def workload_name(wl):
     return f"{wl.name}-B{wl.B}xT{wl.T}xV{wl.V}-{wl.dtype}"
 
 
-def workload_config(wl, g, lanes_per_rank, ws, gc_interval):
+def workload_config(wl, g, lanes_per_rank, ws, gc_interval, lat_interval=0):
     """The `config` object of both arms' JSON lines."""
     # device bytes of the decoder's graph layout: 20 per state (row data,
     # final weight) and 28 per arc (the 16-byte record, source, destination
@@ -256,7 +260,7 @@ def workload_config(wl, g, lanes_per_rank, ws, gc_interval):
     where = f"L2 ({l2_mb:.0f} MB, cudaDevAttrL2CacheSize)" if l2_mb else "L2 (size not queried: no device)"
     l2 = (f"inputs {'larger than' if big else 'against'} {where}: {lp_mb:.0f} MB log-probs per rank, "
           f"{graph_mb:.0f} MB graph; no flush" + ("" if big or l2_mb is None else " (a small case, L2-resident)"))
-    return {"workload": workload_name(wl), "graph": f"{g['num_states']} states / {g['num_arcs']} arcs",
+    cfg = {"workload": workload_name(wl), "graph": f"{g['num_states']} states / {g['num_arcs']} arcs",
             "global_batch": lanes_per_rank * ws, "frames_per_utt": wl.T, "vocab": wl.V,
             "log_probs": wl.dtype, "search_beam": wl.search_beam, "max_active": wl.max_active,
             "min_active": wl.min_active, "parallelism": f"replicas x{ws} (lanes sharded)",
@@ -264,6 +268,9 @@ def workload_config(wl, g, lanes_per_rank, ws, gc_interval):
             "mode": (f"streaming: {wl.chunk}-frame chunks, partial per chunk, finalize with lattice"
                      if wl.streaming else "offline"),
             "gc_interval": gc_interval}
+    if lat_interval:
+        cfg["lat_prune_interval"] = lat_interval
+    return cfg
 
 
 def oracle_sample(wi, threads=None):
@@ -347,7 +354,8 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": DTYPE, "dtype_note": DTYPE_NOTE, "data": "synthetic",
-        "config": workload_config(wl, s["g"], args.lanes or wl.B, args.gpus, args.gc_interval),
+        "config": workload_config(wl, s["g"], args.lanes or wl.B, args.gpus, args.gc_interval,
+                                  args.lat_prune_interval if wl.lattice and wl.streaming else 0),
         "arcs_expanded_per_s": arcs_tot / sum(times),
         "cpu_baseline": dict({"value": value, "unit": "frames/s", "cores": cores, "kind": "oracle",
                               "sample": sample_text(s) + f", {args.steps} timed passes"}, **cpu_extra),
@@ -378,7 +386,8 @@ def run_gpu(args):
     params = W.make_params(wl.search_beam, wl.output_beam, wl.min_active, wl.max_active, True,
                            wl.lattice and wl.streaming and not args.gc_interval, streaming=wl.streaming,
                            options=W.OPT_NO_UB_SKIP if args.no_ub_skip else 0,
-                           gc_interval=args.gc_interval)
+                           gc_interval=args.gc_interval,
+                           lat_prune_interval=args.lat_prune_interval if wl.lattice and wl.streaming else 0)
     nl = args.lanes or wl.B
     caps = W.Capacity(args.frontier_cap, args.log_cap, 0, 0) if (args.log_cap or args.frontier_cap) else None
     D = W.Decoder(G, params, nl, wl.T, caps)
@@ -418,11 +427,11 @@ def run_gpu(args):
                                   W._stream(stream), W._ptr(words), words_cap, W._ptr(wl_), W._ptr(sc),
                                   W._ptr(meta))
             s_ = W.wfst_stats(D.h)
-            tot = s_ if tot is None else {k: (max(tot[k], v) if k == "steps" else tot[k] + v) for k, v in s_.items()}
+            tot = s_ if tot is None else {k: (max(tot[k], v) if k in MAX_STATS else tot[k] + v) for k, v in s_.items()}
         W.wfst_stream_finalize(D.h, W._ptr(chans), B, W._stream(stream), W._ptr(words), words_cap,
                                W._ptr(wl_), W._ptr(sc), W._ptr(meta))
         s_ = W.wfst_stats(D.h)
-        tot = {k: (max(tot[k], v) if k == "steps" else tot[k] + v) for k, v in s_.items()}
+        tot = {k: (max(tot[k], v) if k in MAX_STATS else tot[k] + v) for k, v in s_.items()}
         for c in chans:
             W.wfst_stream_release(D.h, int(c))
         return tot
@@ -478,8 +487,9 @@ def run_gpu(args):
         acc = random_accesses(st0)
         ra = {"accesses": int(acc), "achieved_per_s": acc / kmean_s, "ceiling_per_s": ceil_,
               "frac": acc / kmean_s / ceil_,
-              "counted": "2 per frontier token (recombination entry, arc row) + 1 per admitted candidate "
-                         "(destination entry) + 2 per epsilon arc relaxed",
+              "counted": "2 per frontier token (recombination entry, first arc-row line) + 1 per 8 emitting "
+                         "arcs (further 128-B arc-row lines) + 1 per admitted candidate (destination entry) "
+                         "+ 2 per epsilon arc relaxed",
               "ceiling": "random 16-B / 64-B reads of a 4 GiB table (wfst_probe_random_gather), best of 3"}
     h2d = int(lp_host.nbytes + lens_np.nbytes + 16 * B)
     d2h = int(B * (32 + 64 + 64) + 32 + B * words_cap * 4)
@@ -493,7 +503,8 @@ def run_gpu(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE,
         "dtype_note": DTYPE_NOTE, "data": "synthetic",
-        "config": workload_config(wl, g, B, ws, args.gc_interval),
+        "config": workload_config(wl, g, B, ws, args.gc_interval,
+                                  args.lat_prune_interval if wl.lattice and wl.streaming else 0),
         "arcs_expanded_per_s": arcs_per_s,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": measured_traffic(workload_name(wl), B),
@@ -510,6 +521,7 @@ def run_gpu(args):
         "steps_per_decode": st0["steps"], "barriers_per_decode": st0["barriers"],
         "eps_passes_per_decode": st0["eps_passes"],
         "log_high_water": st0["log_high_water"],
+        "lattice_records_held": st0["lattice_records_held"] if wl.lattice else None,
         "gpu_launches": args.steps * calls_per_step,
         "lanes_ok": res_ok,
         "lanes_overflowed": int((meta[:, 2] != 0).sum()),   # capacity bits left after growth (0 expected)
@@ -540,6 +552,8 @@ def main():
     ap.add_argument("--log-cap", type=int, default=0, help="winners-log entries per lane (0: default)")
     ap.add_argument("--gc-interval", type=int, default=0,
                     help="winners-log GC every N frames per lane (0: off; turns the lattice off)")
+    ap.add_argument("--lat-prune-interval", type=int, default=0,
+                    help="interval lattice prune every N frames (streaming lattice workload; 0: off)")
     args = ap.parse_args()
     if args.steps < 1 or args.warmup < 0:
         ap.error("--steps must be >= 1 and --warmup >= 0")

@@ -125,7 +125,7 @@ typedef struct {
 typedef struct {
   int64_t frontier_cap;   /* tokens per lane per frame (default min(num_states, max(64Ki, 16*max_active))) */
   int64_t log_cap;        /* winners-log entries per lane (default (max_frames+2)*1.5*max_active, >= 1Mi) */
-  int64_t lattice_cap;    /* lattice records per lane (default (max_frames+2)*2*max_active, >= 1Mi) */
+  int64_t lattice_cap;    /* lattice records per lane (default (max_frames+2)*max_active/2, >= 1Mi) */
   int64_t path_cap;       /* arcs of one best path (default 4*(max_frames+2)*(1 + epsilon depth);
                              with the GC, 4*max(max_frames+2, 1024)*(1 + epsilon depth)) */
   int64_t fin_cap;        /* GC only: finalized words per lane (default 65536) */

@@ -462,8 +462,7 @@ extern "C" int wfst_decoder_create(wfst_graph* g, const wfst_params* params, int
   const int64_t fin_cap = gc ? ((caps && caps->fin_cap > 0) ? std::min<int64_t>(caps->fin_cap, kMaxFinCap) : 65536) : 0;
   int64_t lat_cap = 0;
   if (params->lattice)
-    lat_cap = (caps && caps->lattice_cap > 0) ? caps->lattice_cap
-                                              : std::max<int64_t>(mf * 2 * std::max(params->max_active, 1), 1 << 20);
+    lat_cap = (caps && caps->lattice_cap > 0) ? caps->lattice_cap : std::max<int64_t>(mf * ma / 2, 1 << 20);
   // with the GC a backtrack walks only back to the last cut, which can lag
   // the frontier by more than a chunk: room for 4096 frames of arcs
   int64_t path_cap = (caps && caps->path_cap > 0)
