@@ -582,13 +582,19 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
   const int total = S.pre_a[L];
   const LP* lpb = reinterpret_cast<const LP*>(a.lp);
   const int nw = gridDim.x * kWarps;
-  // the CTA's tiles (b*W + j + i*nw for j < W) in order, handed to whichever
-  // of its warps is free by a shared-memory counter
+  // the CTA's tiles, handed in order to whichever of its warps is free by a
+  // shared-memory counter: in each of the R full rounds of nw tiles, the W
+  // adjacent tiles b*W + j + i*nw (j < W); the last, partial round is dealt
+  // out one tile per CTA in turn (tiles R*nw + b + m*G), so that no CTA holds
+  // a whole extra group of W tiles while others have none
+  const int rounds = total / nw;
   for (;;) {
     unsigned c_ = 0;
     if (lane == 0) c_ = atomicAdd(&S.tctr[MODE], 1u);
     c_ = __shfl_sync(0xffffffffu, c_, 0);
-    const int tile = blockIdx.x * kWarps + (int)(c_ % kWarps) + (int)(c_ / kWarps) * nw;
+    const int tile = ((int)c_ < rounds * kWarps)
+                         ? blockIdx.x * kWarps + (int)(c_ % kWarps) + (int)(c_ / kWarps) * nw
+                         : rounds * nw + (int)blockIdx.x + ((int)c_ - rounds * kWarps) * (int)gridDim.x;
     if (tile >= total) break;
     const int l = find_lane(S.pre_a, L, tile);
     const int k = tile - S.pre_a[l];
