@@ -100,6 +100,8 @@ struct Smem {
   float bt_score;
   unsigned long long gc_min;      // GC round: deepest anchor-chain depth another chain met
   int32_t gc_ok, gc_nw;
+  int32_t gc_pre;                 // ancestor GC: the chain walk of the CTA's first task, run
+                                  // during the expand pass (-2: not run)
   unsigned eps_passes;            // epsilon-closure worklist passes of this launch
 };
 
@@ -972,36 +974,51 @@ __device__ bool run_closure(const RunArgs& a, Smem& S, unsigned& epoch) {
 
 // ------------------------------------------------------------------ winners-log GC
 
+// The chain walk of an ancestor-GC cut of lane l at entry E (one thread):
+// follows the winners chain from E down to the root (one load per hop) and
+// keeps its arcs newest first in the lane's path buffer.  Returns the number
+// of arcs, or -1 for no cut (an overflowed lane, an E that is not above the
+// root, a chain longer than the path buffer).  The entries it reads were
+// committed in earlier steps and are not written again before the cut, so
+// the walk may run while the step's expand pass is under way.
+__device__ int gc_walk(const RunArgs& a, const SmLane& s, int l, int64_t E) {
+  const DevWork& w = a.w;
+  int32_t* path = w.path + (size_t)l * (size_t)w.path_cap;
+  const int64_t root = s.floor, hi = s.cursor;
+  if ((__ldcg(&w.lanes[l].overflow) & (kOvfArena | kOvfKept | kOvfPath)) || E <= root || E >= hi) return -1;
+  int n = 0;
+  int64_t i = E;
+  while (i > root && i < hi) {
+    const int2 e = __ldcg(wlog_at(w, l, i));
+    if (e.y < 0) break;
+    if (n >= w.path_cap) return -1;  // longer than the buffer: no cut
+    path[n++] = e.y;
+    i -= sext30((uint32_t)e.x);
+  }
+  return n;
+}
+
 // Cut lane l's winners log at entry E (the whole CTA): the words of the path
 // from the root up to E are appended to the lane's finalized words, E becomes
-// the root (arc -1, no predecessor) and the ring below it is free.  Thread 0
-// follows the chain once (one load per hop), keeping its arcs newest first in
-// the lane's path buffer; the CTA then looks their output labels up and packs
-// the words oldest first.  The kept path of the lane (partial backtracks
-// splice with it) reaches below E, so it is dropped.  Lanes whose log,
-// frontier or path overflowed are left alone, and so is an E that is not
-// above the root or a chain longer than the path buffer.
-__device__ void gc_cut(const RunArgs& a, Smem& S, int l, int64_t E) {
+// the root (arc -1, no predecessor) and the ring below it is free.  The chain
+// walk (gc_walk) is either done here by thread 0 (n_pre = -2) or was done
+// earlier in the step by this CTA's thread 0 (n_pre its result); the CTA
+// then looks the arcs' output labels up and packs the words oldest first.
+// The kept path of the lane (partial backtracks splice with it) reaches below
+// E, so it is dropped.  Lanes whose log, frontier or path overflowed are left
+// alone.
+__device__ void gc_cut(const RunArgs& a, Smem& S, int l, int64_t E, int n_pre) {
   const DevWork& w = a.w;
   const DevGraph& g = a.g;
   const SmLane& s = S.lane[l];
   const int tid = threadIdx.x;
   int32_t* path = w.path + (size_t)l * (size_t)w.path_cap;
   if (tid == 0) {
-    const int64_t root = s.floor, hi = s.cursor;
-    int n = -1;
-    if (!(__ldcg(&w.lanes[l].overflow) & (kOvfArena | kOvfKept | kOvfPath)) && E > root && E < hi) {
+    int n = n_pre >= -1 ? n_pre : gc_walk(a, s, l, E);
+    if (__ldcg(&w.lanes[l].overflow) & (kOvfArena | kOvfKept | kOvfPath)) n = -1;
+    if (n >= 0) {
       w.lanes[l].bt_top = -1;
       w.lanes[l].bt_len = 0;
-      n = 0;
-      int64_t i = E;
-      while (i > root && i < hi) {
-        const int2 e = __ldcg(wlog_at(w, l, i));
-        if (e.y < 0) break;
-        if (n >= w.path_cap) { n = -1; break; }  // longer than the buffer: no cut
-        path[n++] = e.y;
-        i -= sext30((uint32_t)e.x);
-      }
     }
     S.bt_n = n;
   }
@@ -1149,7 +1166,7 @@ __device__ void gc_round(const RunArgs& a, Smem& S, int l) {
   }
   __threadfence();
   __syncthreads();
-  if (run && S.gc_ok) gc_cut(a, S, l, S.bt_idx);
+  if (run && S.gc_ok) gc_cut(a, S, l, S.bt_idx, -2);
   __syncthreads();
 }
 
@@ -1888,11 +1905,30 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         if (s.expanded) S.pre_a[l] = (int32_t)((s.d_cur + kTile - 1) / kTile);
       }
     }
+    // the step's end-of-step tasks (final step, partial, GC round), one per
+    // lane with a task, the task-th going to CTA task mod G
+    for (int l = tid; l < L; l += kThreads)
+      S.pre_b[l] = (S.lane[l].phase == kFin || S.lane[l].phase == kPart || S.lane[l].gc_due) ? 1 : 0;
     __syncthreads();
     lane_scan(S.pre_a, L);
+    lane_scan(S.pre_b, L);
     if (blockIdx.x == 0 && g.has_eps)
       for (int l = tid; l < L; l += kThreads)
         if (S.lane[l].phase == kEmit) w.wl_cnt[(size_t)1 * L + l] = 0ull;
+    if (ANC) {
+      // the chain walk of this CTA's first task, when that is a GC cut, runs
+      // now in thread 0 while the CTA's other warps start on the expand
+      // tiles (warp 0 joins them after the walk): its serial loads overlap
+      // the pass instead of holding the step's end
+      if (tid == 0) {
+        S.gc_pre = -2;
+        if ((int)blockIdx.x < S.pre_b[L]) {
+          const int l = find_lane(S.pre_b, L, (int)blockIdx.x);
+          if (S.lane[l].gc_due) S.gc_pre = gc_walk(a, S.lane[l], l, S.lane[l].gc_e);
+        }
+      }
+      __syncwarp();
+    }
     emit_tiles<1, LP, ANC>(a, S);
     prof_mark(prof, tsub, kProfExpTiles);
 
@@ -1929,10 +1965,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     }
 
     {  // final step (§3) / partial (§8): one CTA per lane walks the winners log
-      for (int l = tid; l < L; l += kThreads)
-        S.pre_b[l] = (S.lane[l].phase == kFin || S.lane[l].phase == kPart || S.lane[l].gc_due) ? 1 : 0;
       __syncthreads();
-      lane_scan(S.pre_b, L);
       const int ntask = S.pre_b[L];
       for (int task = blockIdx.x; task < ntask; task += G) {
         const int l = find_lane(S.pre_b, L, task);
@@ -1940,7 +1973,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         const int f = s.t, par = f & 1;
         if (s.gc_due) {
           if (ANC) {
-            gc_cut(a, S, l, s.gc_e);
+            gc_cut(a, S, l, s.gc_e, task == (int)blockIdx.x ? S.gc_pre : -2);
             __syncthreads();  // the CTA's next task reuses the path scan space
           } else {
             gc_round(a, S, l);
