@@ -462,13 +462,16 @@ def run_gpu(args):
     if dist:
         dist.barrier()
     ms = ev0.elapsed_time(ev1)
-    # end to end through the C ABI with pinned host buffers (H2D inside the call)
+    clk = clocks.stop()
+    # end to end through the C ABI with pinned host buffers (H2D inside the
+    # call); one untimed call first, which sets up the decoder's staging
+    # buffer for host input
+    step(True)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         step(True)
     e2e_s = time.perf_counter() - t0
-    clk = clocks.stop()
     frames_step = int(lens.sum())
     st0 = stats[0]
     assert all(s["frames"] == st0["frames"] and s["arcs_expanded"] == st0["arcs_expanded"] for s in stats)
