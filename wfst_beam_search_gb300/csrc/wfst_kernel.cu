@@ -40,6 +40,12 @@ constexpr int kCB = 5;                                     // tokens per thread 
 
 enum Phase { kNone = 0, kEmit = 1, kFin = 2, kPart = 3 };
 
+// Kernel instantiations.  The epsilon closure, lattices and the walking GC
+// round live in the general one only; a decode of an epsilon-free graph
+// without lattices runs a kernel with that code compiled out (its registers
+// then serve the emitting passes), with or without the ancestor GC.
+enum Kind { kKindGeneral = 0, kKindPlain = 1, kKindAnc = 2 };
+
 struct SmLane {
   int32_t t, committed, status, phase;
   float beam, cutoff;
@@ -521,14 +527,14 @@ __device__ __forceinline__ void warp_append(const bool (&want)[K], const int32_t
 
 // Claim states into frame f of lane l (and seed the epsilon worklist W0 with
 // the claimed states that have epsilon arcs).
-template <int K>
+template <int K, bool GEN = true>
 __device__ __forceinline__ void warp_claim(const RunArgs& a, const bool (&want)[K], const int32_t (&d)[K],
                                            int l, int f, bool seed_worklist) {
   const DevWork& w = a.w;
   const int par = f & 1;
   warp_append<K, false>(want, d, &fc_of(w, f, l)->cnt, w.front + ql(w, par, l), w.tile_first + tl(w, par, l),
-                        tpos_kept(a) ? par : -1, w.qcap, a, l);
-  if (a.g.has_eps && seed_worklist) {
+                        (GEN && tpos_kept(a)) ? par : -1, w.qcap, a, l);
+  if (GEN && a.g.has_eps && seed_worklist) {
     bool ws[K];
 #pragma unroll
     for (int k = 0; k < K; k++) {
@@ -574,10 +580,13 @@ __device__ __forceinline__ void lat_put(const RunArgs& a, int l, unsigned long l
 //   stages every token's score for MODE 1.
 // MODE 1 (expand): admission against the cutoff + recombination into the
 //   next frame.
-template <int MODE, typename LP, bool ANC>
+template <int MODE, typename LP, int KIND>
 __device__ void emit_tiles(const RunArgs& a, Smem& S) {
+  constexpr bool ANC = KIND == kKindAnc;
+  constexpr bool GEN = KIND == kKindGeneral;  // epsilon arcs and lattices possible
   const DevWork& w = a.w;
   const DevGraph& g = a.g;
+  const bool lat = GEN && a.lattice;
   const int L = a.nlanes;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   WStage& ws = S.ws[warp];
@@ -643,7 +652,7 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
             // a token that no other tile stages is cleared right after its
             // read (its line is in L2 now); the first token of tile k > 0 is
             // also staged by tile k-1 and is cleared by the expand pass
-            if (!a.lattice && p < own_hi && (p > p_lo || k == 0))
+            if (!lat && p < own_hi && (p > p_lo || k == 0))
               *ent_at(w, l, tr.state, par) = make_ulonglong2(0ull, 0ull);
             if (s.need_commit && p < own_hi) {
               // commit (§5.4): the winners-log entry {delta, arc} of the token
@@ -652,7 +661,7 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
               const int64_t base_new = s.cursor, base_old = s.base_cur;
               const int64_t prev = ((src >> 31) ? base_new : base_old) + (src & 0x7fffffffu);
               wlog_commit(a, l, base_new + p, s.floor, arc, prev);
-              if (g.has_eps) {
+              if (GEN && g.has_eps) {
                 const int4 m = __ldg(g.meta + tr.state);
                 if (m.z > m.y) atomicAdd(&w.stats[l].eps, (unsigned long long)(m.z - m.y));
               }
@@ -667,7 +676,7 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
             sc = __ldcg(w.score + q + c + i);
             if (ANC) ws.tpos[i] = __ldcg(w.anc + q + c + i);  // the token's checkpoint ancestor
             // entries the max pass left (lattices, tile-boundary tokens)
-            if (a.lattice || (c + i == p_lo && k > 0))
+            if (lat || (c + i == p_lo && k > 0))
               *ent_at(w, l, tr.state, par) = make_ulonglong2(0ull, 0ull);
           }
           ws.off[i] = tr.off;
@@ -717,7 +726,7 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
       for (int j = 0; j < kSPT; j++) {
         const float lpv = act[j] ? lp_at<LP>(row, il[j]) : 0.f;
         end[j] = act[j] ? __fadd_rn(__fadd_rn(ws.score[ti[j]], wt[j]), lpv) : -INFINITY;
-        if (MODE == 1 && a.lattice) wt[j] = __fadd_rn(wt[j], lpv);  // the record's own score
+        if (MODE == 1 && lat) wt[j] = __fadd_rn(wt[j], lpv);  // the record's own score
       }
       if (MODE == 0) {
 #pragma unroll
@@ -755,7 +764,7 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
             }
           }
         }
-        if (a.lattice) {
+        if (lat) {
           unsigned lm[kSPT];
           unsigned long long lb = warp_lat_reserve<kSPT>(a, adm, l, lm);
           const unsigned lt = lanemask_lt();
@@ -790,7 +799,7 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
           claim[j] = adm[j] && relax_ent(a, ent_at(w, l, d[j], par ^ 1), mk_key(end[j], id[j]), srcw) == 2;
           admitted += adm[j] ? 1u : 0u;
         }
-        warp_claim<kSPT>(a, claim, d, l, f + 1, true);
+        warp_claim<kSPT, GEN>(a, claim, d, l, f + 1, true);
       }
     }
     if (MODE == 0) {
@@ -1521,11 +1530,14 @@ __device__ inline void smem_carve(Smem& S, unsigned char* raw, int L) {
   S.glo = reinterpret_cast<int64_t*>(p);
 }
 
-// ANC: the ancestor GC is on (the winners-log GC of an epsilon-free graph);
-// a separate instantiation, so that decodes without it carry none of its
-// registers.
-template <typename LP, bool ANC>
+// KIND (see Kind): kKindAnc runs the ancestor GC (the winners-log GC of an
+// epsilon-free graph), kKindPlain an epsilon-free graph without lattices or
+// GC, kKindGeneral everything else; separate instantiations, so that each
+// carries only the registers its own code needs.
+template <typename LP, int KIND>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
+  constexpr bool ANC = KIND == kKindAnc;
+  constexpr bool GEN = KIND == kKindGeneral;  // epsilon arcs, lattices, the walking GC round
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   if (threadIdx.x == 0) smem_carve(S, smem_raw, a.nlanes);
@@ -1537,7 +1549,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
   const int G = gridDim.x;
   const int64_t gstride = (int64_t)G * kThreads;
   const int64_t gstart = (int64_t)blockIdx.x * kThreads + tid;
-  const bool lat = a.lattice != 0;
+  const bool lat = GEN && a.lattice != 0;
   unsigned epoch = 0;
   unsigned long long steps = 0;
   unsigned long long* prof = S.prof;
@@ -1616,7 +1628,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
         if (S.lane[l].flags & kCallInit) init_lane_global(a, l);
     row_maxima<LP>(a, S);
     if (!grid_sync(a, S, epoch)) return;
-    if (S.any && g.has_eps) {
+    if (S.any && (GEN && g.has_eps)) {
       for (int l = tid; l < L; l += kThreads) {
         SmLane& s = S.lane[l];
         s.closure = (s.flags & kCallInit) ? 1 : 0;  // frame 0
@@ -1718,7 +1730,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
           FrameCnt z;
           z.cnt = 0; z.maxkey = 0; z.admitted = 0; z.final_key = 0; z.best_key = 0; z.anc_hi = 0; z.anc_lo = 0;
           *fc_of(w, s.t + 1, l) = z;
-          if (g.has_eps) w.wl_cnt[l] = 0ull;
+          if (GEN && g.has_eps) w.wl_cnt[l] = 0ull;
         }
         if (lat && s.phase != kNone && s.need_commit)
           w.lat_groups[(size_t)l * (w.max_frames + 2) + s.t] = s.res_hi;
@@ -1768,7 +1780,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
             // the winner's source token: same frame for an epsilon arc, else the previous one
             const int64_t prev = ((src[k] >> 31) & 1ull ? base_new : base_old) + (int64_t)(src[k] & 0x7fffffffull);
             wlog_commit(a, l, base_new + pk[k], s.floor, arc, prev);
-            if (g.has_eps) {
+            if (GEN && g.has_eps) {
               const int4 m = __ldg(g.meta + st[k]);
               if (m.z > m.y) atomicAdd(&w.stats[l].eps, (unsigned long long)(m.z - m.y));
             }
@@ -1835,7 +1847,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
       }
     }
     prof_mark(prof, tsub, kProfClear);
-    emit_tiles<0, LP, ANC>(a, S);
+    emit_tiles<0, LP, KIND>(a, S);
     prof_mark(prof, tsub, kProfMaxTiles);
     if (!grid_sync(a, S, epoch)) return;
     prof_mark(prof, tsub, kProfBarX);
@@ -1892,7 +1904,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
           }
         }
       } else {
-        s.gc_due = (a.gc_interval > 0 && s.phase == kEmit && s.n_cur > 0 && s.t + 1 - s.gc_t >= a.gc_interval)
+        s.gc_due = (GEN && a.gc_interval > 0 && s.phase == kEmit && s.n_cur > 0 &&
+                    s.t + 1 - s.gc_t >= a.gc_interval)
                        ? 1 : 0;
         if (s.gc_due) s.gc_t = s.t + 1;
       }
@@ -1912,7 +1925,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     __syncthreads();
     lane_scan(S.pre_a, L);
     lane_scan(S.pre_b, L);
-    if (blockIdx.x == 0 && g.has_eps)
+    if (blockIdx.x == 0 && (GEN && g.has_eps))
       for (int l = tid; l < L; l += kThreads)
         if (S.lane[l].phase == kEmit) w.wl_cnt[(size_t)1 * L + l] = 0ull;
     if (ANC) {
@@ -1929,7 +1942,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
       }
       __syncwarp();
     }
-    emit_tiles<1, LP, ANC>(a, S);
+    emit_tiles<1, LP, KIND>(a, S);
     prof_mark(prof, tsub, kProfExpTiles);
 
     // final-arc lattice records (read the entries; cleared only after the loop)
@@ -1975,7 +1988,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
           if (ANC) {
             gc_cut(a, S, l, s.gc_e, task == (int)blockIdx.x ? S.gc_pre : -2);
             __syncthreads();  // the CTA's next task reuses the path scan space
-          } else {
+          } else if (GEN) {
             gc_round(a, S, l);
           }
           continue;
@@ -2001,7 +2014,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
           S.bt_score = score;
           S.bt_n = -1;   // the token's position in frame f, when kept
           S.bt_pad = -1; // ... else found by the scan below
-          if (ok && tpos_kept(a)) S.bt_n = __ldcg(tpos_at(w, l, state, par));
+          if (ok && GEN && tpos_kept(a)) S.bt_n = __ldcg(tpos_at(w, l, state, par));
         }
         __syncthreads();
         if (S.bt_ok && S.bt_n < 0) {
@@ -2150,7 +2163,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
     prof_mark(prof, tlast, kProfExpand);
 
     // ================= epsilon closure of the new frames (§5.5)
-    if (g.has_eps) {
+    if (GEN && g.has_eps) {
       for (int l = tid; l < L; l += kThreads) {
         SmLane& s = S.lane[l];
         s.closure = (s.phase == kEmit && s.expanded) ? s.t + 2 : 0;  // frame t+1
@@ -2256,36 +2269,44 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
 
 size_t smem_bytes(int L) { return smem_size(L); }
 
-template <typename LP, bool ANC>
+template <typename LP, int KIND>
 static cudaError_t prepare_t() {
-  return cudaFuncSetAttribute(decode_kernel<LP, ANC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(decode_kernel<LP, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)smem_size(kMaxLanes));
 }
 
-template <typename LP, bool ANC>
+template <typename LP, int KIND>
 static cudaError_t launch_t(const RunArgs& a, int grid, cudaStream_t st) {
   void* args[] = {(void*)&a};
-  cudaError_t e = prepare_t<LP, ANC>();
+  cudaError_t e = prepare_t<LP, KIND>();
   if (e != cudaSuccess) return e;
-  return cudaLaunchCooperativeKernel((const void*)decode_kernel<LP, ANC>, dim3(grid), dim3(kThreads), args,
+  return cudaLaunchCooperativeKernel((const void*)decode_kernel<LP, KIND>, dim3(grid), dim3(kThreads), args,
                                      smem_size(a.nlanes), st);
 }
 
-cudaError_t launch_decode(const RunArgs& a, int dtype, int grid, cudaStream_t st) {
-  const bool anc = a.gc_interval > 0 && a.w.anc != nullptr;
-  if (dtype == 1) return anc ? launch_t<__half, true>(a, grid, st) : launch_t<__half, false>(a, grid, st);
-  return anc ? launch_t<float, true>(a, grid, st) : launch_t<float, false>(a, grid, st);
+// The instantiation a call runs: the ancestor GC (an epsilon-free graph with
+// its ancestor table), the plain kernel (epsilon-free, no lattice, no GC) or
+// the general one.
+template <typename LP>
+static cudaError_t launch_kind(const RunArgs& a, int grid, cudaStream_t st) {
+  if (a.gc_interval > 0 && a.w.anc != nullptr) return launch_t<LP, kKindAnc>(a, grid, st);
+  if (!a.g.has_eps && !a.lattice && a.gc_interval == 0) return launch_t<LP, kKindPlain>(a, grid, st);
+  return launch_t<LP, kKindGeneral>(a, grid, st);
 }
 
-template <typename LP, bool ANC>
+cudaError_t launch_decode(const RunArgs& a, int dtype, int grid, cudaStream_t st) {
+  return dtype == 1 ? launch_kind<__half>(a, grid, st) : launch_kind<float>(a, grid, st);
+}
+
+template <typename LP, int KIND>
 static cudaError_t occupancy_t(size_t sm, int* per) {
-  cudaError_t e = prepare_t<LP, ANC>();
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(per, decode_kernel<LP, ANC>, kThreads, sm);
+  cudaError_t e = prepare_t<LP, KIND>();
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(per, decode_kernel<LP, KIND>, kThreads, sm);
   return e;
 }
 
 // Cooperative grid for a launch over L lanes: resident CTAs per SM x SMs
-// (the smaller of the two instantiations, so that either fits the grid).
+// (the smallest over the instantiations, so that each fits the grid).
 cudaError_t max_grid(int dtype, int L, int* grid) {
   int dev = 0, sms = 0, p0 = 0, p1 = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -2293,15 +2314,18 @@ cudaError_t max_grid(int dtype, int L, int* grid) {
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const size_t sm = smem_size(L);
+  int p2 = 0;
   if (dtype == 1) {
-    e = occupancy_t<__half, false>(sm, &p0);
-    if (e == cudaSuccess) e = occupancy_t<__half, true>(sm, &p1);
+    e = occupancy_t<__half, kKindGeneral>(sm, &p0);
+    if (e == cudaSuccess) e = occupancy_t<__half, kKindAnc>(sm, &p1);
+    if (e == cudaSuccess) e = occupancy_t<__half, kKindPlain>(sm, &p2);
   } else {
-    e = occupancy_t<float, false>(sm, &p0);
-    if (e == cudaSuccess) e = occupancy_t<float, true>(sm, &p1);
+    e = occupancy_t<float, kKindGeneral>(sm, &p0);
+    if (e == cudaSuccess) e = occupancy_t<float, kKindAnc>(sm, &p1);
+    if (e == cudaSuccess) e = occupancy_t<float, kKindPlain>(sm, &p2);
   }
   if (e != cudaSuccess) return e;
-  *grid = std::min(p0, p1) * sms;
+  *grid = std::min(p0, std::min(p1, p2)) * sms;
   return cudaSuccess;
 }
 
