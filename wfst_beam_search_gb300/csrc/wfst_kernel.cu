@@ -284,29 +284,33 @@ __device__ __forceinline__ void prof_mark(unsigned long long* acc, int from, int
 // Bounded software grid barrier.  Returns false when the launch aborts.  A
 // wait gives up after a.timeout_ns; a.bar_extra (0 except under the test
 // hook that exercises this path) raises the arrival target beyond the grid.
+// The arrival is a release add at GPU scope (after the CTA barrier, it
+// publishes every write of the CTA), the wait an acquire load of the count
+// (it sees every write the other CTAs published); the abort flag and the
+// time limit are looked at every 16 polls.
 __device__ bool grid_sync(const RunArgs& a, Smem& S, unsigned& epoch) {
   __syncthreads();
   if (threadIdx.x == 0) {
     GridBar* bar = a.w.bar;
     epoch++;
     const unsigned target = epoch * (unsigned)gridDim.x + a.bar_extra;
-    __threadfence();
-    atomicAdd(&bar->count, 1u);
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" : : "l"(&bar->count) : "memory");
     int ab = 0;
     const unsigned long long t0 = gtimer();
-    for (;;) {
+    for (unsigned it = 1;; it++) {
       const unsigned c = ld_acquire(&bar->count);
       if ((int)(c - target) >= 0) break;
-      if (ld_acquire(&bar->abort)) { ab = 1; break; }
-      if (gtimer() - t0 > a.timeout_ns) {
-        atomicExch(&bar->abort, 1u);
-        atomicOr(&bar->error, 1u);
-        ab = 1;
-        break;
+      if ((it & 15u) == 0u) {
+        if (ld_acquire(&bar->abort)) { ab = 1; break; }
+        if (gtimer() - t0 > a.timeout_ns) {
+          atomicExch(&bar->abort, 1u);
+          atomicOr(&bar->error, 1u);
+          ab = 1;
+          break;
+        }
       }
       __nanosleep(32);
     }
-    __threadfence();
     S.abort = ab;
   }
   __syncthreads();
