@@ -809,7 +809,8 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
     if (MODE == 0) {
       for (int o = 16; o; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
       if (lane == 0 && vmax > -INFINITY) atomicMax(&fc_of(w, f, l)->maxkey, ord_f(vmax));
-      if (ANC) anc_post(a, l, f, amin, amax);
+      // the frame's ancestor bounds are read only at the GC's check frames
+      if (ANC && f % a.gc_interval == 0) anc_post(a, l, f, amin, amax);
     } else {
       for (int o = 16; o; o >>= 1) admitted += __shfl_xor_sync(0xffffffffu, admitted, o);
       if (lane == 0 && admitted) atomicAdd(&w.stats[l].sum_a, (unsigned long long)admitted);
@@ -1791,9 +1792,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
             if (ANC) {
               const int32_t an = anc_of(f, arc, src[k], s.gc_c);
               w.anc[ql(w, f & 1, l) + pk[k]] = an;
-              FrameCnt* fc = fc_of(w, f, l);
-              atomicMax(&fc->anc_hi, (unsigned)(an + 1));
-              atomicMax(&fc->anc_lo, 0x7fffffffu - (unsigned)an);
+              if (f % a.gc_interval == 0) {  // bounds read at the GC's check frames only
+                FrameCnt* fc = fc_of(w, f, l);
+                atomicMax(&fc->anc_hi, (unsigned)(an + 1));
+                atomicMax(&fc->anc_lo, 0x7fffffffu - (unsigned)an);
+              }
             }
           }
           if (s.phase == kFin) {
