@@ -639,6 +639,7 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
     float vmax = -INFINITY;
     uint32_t admitted = 0;
     int32_t amin = 0x7fffffff, amax = -1;  // ancestor GC: the tile's committed tokens' ancestors
+    uint32_t eps_n = 0;                    // epsilon arcs of the tile's committed tokens (statistic)
     for (int32_t c = p_lo; c < p_hi; c += kTokCap) {
       const int ntok = min(kTokCap, p_hi - c);
       __syncwarp();
@@ -667,7 +668,7 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
               wlog_commit(a, l, base_new + p, s.floor, arc, prev);
               if (GEN && g.has_eps) {
                 const int4 m = __ldg(g.meta + tr.state);
-                if (m.z > m.y) atomicAdd(&w.stats[l].eps, (unsigned long long)(m.z - m.y));
+                eps_n += (uint32_t)(m.z - m.y);
               }
               if (ANC) {
                 const int32_t an = anc_of(f, arc, e.y, s.gc_c);
@@ -809,6 +810,10 @@ __device__ void emit_tiles(const RunArgs& a, Smem& S) {
     if (MODE == 0) {
       for (int o = 16; o; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
       if (lane == 0 && vmax > -INFINITY) atomicMax(&fc_of(w, f, l)->maxkey, ord_f(vmax));
+      if (GEN && g.has_eps) {  // one atomic per tile, not per token
+        for (int o = 16; o; o >>= 1) eps_n += __shfl_xor_sync(0xffffffffu, eps_n, o);
+        if (lane == 0 && eps_n) atomicAdd(&w.stats[l].eps, (unsigned long long)eps_n);
+      }
       // the frame's ancestor bounds are read only at the GC's check frames
       if (ANC && f % a.gc_interval == 0) anc_post(a, l, f, amin, amax);
     } else {
