@@ -1769,12 +1769,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
           pk[k] = v[k] ? gi - S.pre_b[lk[k]] : 0;
           st[k] = v[k] ? __ldcg(&w.front[ql(w, S.lane[lk[k]].t & 1, lk[k]) + pk[k]].state) : 0;
         }
-        unsigned long long src[kCB];
+        unsigned long long src[kCB], fkey[kCB], bkey[kCB];
 #pragma unroll
         for (int k = 0; k < kCB; k++) {
           const ulonglong2 e = v[k] ? __ldcg(ent_at(w, lk[k], st[k], S.lane[lk[k]].t & 1)) : make_ulonglong2(0, 0);
           key[k] = e.x;
           src[k] = e.y;
+          fkey[k] = bkey[k] = 0ull;
         }
 #pragma unroll
         for (int k = 0; k < kCB; k++) {
@@ -1806,12 +1807,40 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
           }
           if (s.phase == kFin) {
             const float fw = __ldg(g.final_w + st[k]);
-            if (fw > -INFINITY) {
-              atomicMax(&fc_of(w, f, l)->final_key, mk_key(__fadd_rn(score, fw), st[k]));
+            if (fw > -INFINITY) fkey[k] = mk_key(__fadd_rn(score, fw), st[k]);
+          }
+          if (s.phase == kFin || s.phase == kPart) bkey[k] = key[k];
+        }
+        // final-step keys, finals count and best key: reduced over the warp
+        // first when its tokens of a slot all belong to one lane (the usual
+        // case), so that a lane's address takes one atomic per warp, not per
+        // token
+#pragma unroll
+        for (int k = 0; k < kCB; k++) {
+          const int l = lk[k];
+          const int l0 = __shfl_sync(0xffffffffu, l, 0);
+          unsigned long long fk = fkey[k], bk = bkey[k];
+          if (__all_sync(0xffffffffu, !v[k] || l == l0)) {
+            uint32_t nf = fk ? 1u : 0u;
+            for (int o = 16; o; o >>= 1) {
+              fk = max(fk, __shfl_xor_sync(0xffffffffu, fk, o));
+              bk = max(bk, __shfl_xor_sync(0xffffffffu, bk, o));
+              nf += __shfl_xor_sync(0xffffffffu, nf, o);
+            }
+            if ((tid & 31) == 0) {
+              const int f0 = S.lane[l0].t;
+              if (fk) atomicMax(&fc_of(w, f0, l0)->final_key, fk);
+              if (nf) atomicAdd(&w.stats[l0].finals, (unsigned long long)nf);
+              if (bk) atomicMax(&fc_of(w, f0, l0)->best_key, bk);
+            }
+          } else if (v[k]) {
+            const int f = S.lane[l].t;
+            if (fk) {
+              atomicMax(&fc_of(w, f, l)->final_key, fk);
               atomicAdd(&w.stats[l].finals, 1ull);
             }
+            if (bk) atomicMax(&fc_of(w, f, l)->best_key, bk);
           }
-          if (s.phase == kFin || s.phase == kPart) atomicMax(&fc_of(w, f, l)->best_key, key[k]);
         }
       }
     }
