@@ -836,7 +836,10 @@ __device__ void eps_tiles(const RunArgs& a, Smem& S, int buf, int next_slot) {
   WStage& ws = S.ws[warp];
   const int total = S.pre_a[L];
   const int nw = gridDim.x * kWarps;
-  for (int tile = blockIdx.x * kWarps + warp; tile < total; tile += nw) {
+  // tiles dealt out across the CTAs first (tile t to CTA t mod G, warp
+  // t / G of each round), so that a pass smaller than the grid spreads over
+  // every SM instead of filling the first CTAs' warps
+  for (int tile = warp * (int)gridDim.x + (int)blockIdx.x; tile < total; tile += nw) {
     const int l = find_lane(S.pre_a, L, tile);
     const int k = tile - S.pre_a[l];
     const SmLane& s = S.lane[l];
