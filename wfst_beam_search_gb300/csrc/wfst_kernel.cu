@@ -1870,24 +1870,43 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const RunArgs a) {
       }
     }
     if (lat) {  // lattice records of the last step: resolve their frame-t tokens
+      // (two records per thread at a time, so that their dependent reads
+      // overlap)
       const int total = S.pre_d[L];
-      for (int gi = (int)gstart; gi < total; gi += (int)gstride) {
-        const int l = find_lane(S.pre_d, L, gi);
-        const SmLane& s = S.lane[l];
-        const int64_t r = s.res_lo + (gi - S.pre_d[l]);
-        LatRec* rp = w.lat + (size_t)l * w.lat_stride + r;
-        LatRec rec = *rp;
-        const int par = s.t & 1;
-        const int64_t base_new = s.cursor;  // frame t
-        rec.dst_tok = (int32_t)(base_new + __ldcg(tpos_at(w, l, rec.dst_state, par)));
-        if (rec.frame_flags & kRecEps) {
-          // keep only the relaxation evaluated with the source's final score
-          const unsigned used = (unsigned)rec.src_tok;
-          const float fin = key_score(__ldcg(&ent_at(w, l, rec.src_state, par)->x));
-          rec.src_tok = (int32_t)(base_new + __ldcg(tpos_at(w, l, rec.src_state, par)));
-          if (ord_f(__uint_as_float(used)) != ord_f(fin)) rec.frame_flags |= kRecDead;
+      for (int g0 = (int)gstart; g0 < total; g0 += (int)gstride * 2) {
+        const int g1 = g0 + (int)gstride;
+        const int l0 = find_lane(S.pre_d, L, g0);
+        const int l1 = g1 < total ? find_lane(S.pre_d, L, g1) : l0;
+        LatRec* r0 = w.lat + (size_t)l0 * w.lat_stride + (S.lane[l0].res_lo + (g0 - S.pre_d[l0]));
+        LatRec* r1 = w.lat + (size_t)l1 * w.lat_stride + (S.lane[l1].res_lo + (g1 - S.pre_d[l1]));
+        int4 h0 = __ldcg(reinterpret_cast<const int4*>(r0));
+        const int32_t d0 = __ldcg(&r0->dst_state);
+        int4 h1 = make_int4(0, 0, 0, 0);
+        int32_t d1 = 0;
+        if (g1 < total) {
+          h1 = __ldcg(reinterpret_cast<const int4*>(r1));
+          d1 = __ldcg(&r1->dst_state);
         }
-        *rp = rec;
+        const int p0 = S.lane[l0].t & 1, p1 = S.lane[l1].t & 1;
+        const int32_t t0 = __ldcg(tpos_at(w, l0, d0, p0));
+        const int32_t t1 = g1 < total ? __ldcg(tpos_at(w, l1, d1, p1)) : 0;
+        h0.z = (int32_t)(S.lane[l0].cursor + t0);
+        h1.z = (int32_t)(S.lane[l1].cursor + t1);
+        if (h0.x & kRecEps) {
+          // keep only the relaxation evaluated with the source's final score
+          const unsigned used = (unsigned)h0.y;
+          const float fin = key_score(__ldcg(&ent_at(w, l0, h0.w, p0)->x));
+          h0.y = (int32_t)(S.lane[l0].cursor + __ldcg(tpos_at(w, l0, h0.w, p0)));
+          if (ord_f(__uint_as_float(used)) != ord_f(fin)) h0.x |= kRecDead;
+        }
+        if (g1 < total && (h1.x & kRecEps)) {
+          const unsigned used = (unsigned)h1.y;
+          const float fin = key_score(__ldcg(&ent_at(w, l1, h1.w, p1)->x));
+          h1.y = (int32_t)(S.lane[l1].cursor + __ldcg(tpos_at(w, l1, h1.w, p1)));
+          if (ord_f(__uint_as_float(used)) != ord_f(fin)) h1.x |= kRecDead;
+        }
+        *reinterpret_cast<int4*>(r0) = h0;
+        if (g1 < total) *reinterpret_cast<int4*>(r1) = h1;
       }
     }
     prof_mark(prof, tsub, kProfClear);
