@@ -22,10 +22,12 @@
 //   §5.5 epsilon closure by worklist passes to a fixpoint; lattice records;
 //   §7  backtrack from the final token; lattice backward output_beam prune.
 // Work distribution: the arc slots of a frame form tiles of kTile slots; a
-// CTA owns every (G*W)-th group of W adjacent tiles (W warps per CTA) and
-// hands them, in order, to whichever of its warps is free; a warp stages its
-// tile's tokens in its own shared-memory area, and every lane issues the
-// loads of its kSPT slots together (one chain of dependent accesses per tile).
+// CTA owns every (G*W)-th group of W adjacent tiles (W warps per CTA), the
+// last partial round dealt out one tile per CTA, and hands them, in order,
+// to whichever of its warps is free; a warp stages its tile's tokens in its
+// own shared-memory area, and every lane issues the loads of its kSPT slots
+// together (one chain of dependent accesses per tile).
+// Three instantiations (Kind) compile only the code their decodes need.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
