@@ -935,13 +935,26 @@ __device__ void eps_tiles(const RunArgs& a, Smem& S, int buf, int next_slot) {
         better[j] = r >= 1;
       }
       warp_claim<kSPT>(a, claim, d, l, fr, false);
+      // improved states with epsilon arcs go to the next worklist once per
+      // pass (the mark); a state this warp claimed is new in the frame, so
+      // it is appended without waiting for the mark's old value (a later
+      // improvement by another warp that misses the store appends it again:
+      // the next pass relaxes it twice with the same score)
       bool wl[kSPT];
 #pragma unroll
       for (int j = 0; j < kSPT; j++) {
         wl[j] = false;
         if (better[j]) {
           const int4 m = __ldg(g.meta + d[j]);
-          if (m.z > m.y) wl[j] = atomicExch(w.mark + (size_t)l * w.N + d[j], pass_id) != pass_id;
+          if (m.z > m.y) {
+            uint32_t* mk = w.mark + (size_t)l * w.N + d[j];
+            if (claim[j]) {
+              *mk = pass_id;
+              wl[j] = true;
+            } else {
+              wl[j] = atomicExch(mk, pass_id) != pass_id;
+            }
+          }
         }
       }
       warp_append<kSPT, true>(wl, d, &w.wl_cnt[(size_t)next_slot * L + l], w.wl + ql(w, buf ^ 1, l),
